@@ -1,0 +1,203 @@
+/*
+ * CPU oracle for the fused gated activations -- TEST INFRASTRUCTURE ONLY.
+ *
+ * Only the test suite, the smoke check and the CPU-baseline leg of the
+ * benchmark may load this file's library.  The CUDA library never links,
+ * includes or calls it, and it shares no code with the CUDA library.
+ *
+ * Everything here is plain fp64 C written straight from the definitions, one
+ * loop per stage, with no blocking, fusion or reordering:
+ *
+ *  gelu_and_mul_sparse  -- vLLM PR "[Performance] Add Triton kernel for
+ *      Gemma3n sparse GELU", section "Purpose": the activation takes per-row
+ *      mean and variance, a Gaussian threshold, tanh GELU and the gated
+ *      multiplication.  Reading of each stage (the page names the stages but
+ *      prints no formula):
+ *        gate g = columns [0, d) of the row, up u = columns [d, 2d);
+ *        mean   = sum_j g_j / d;
+ *        var    = sum_j (g_j - mean)^2 / d       (population variance);
+ *        cutoff = mean + sqrt(var) * z,  z = inverse normal CDF of the target
+ *                 sparsity (passed in; 0.95 gives z = 1.6448536269514722);
+ *        s_j    = max(g_j - cutoff, 0);
+ *        out_j  = gelu_tanh(s_j) * u_j,
+ *        gelu_tanh(x) = 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3)))
+ *                 (the tanh form of GELU of Hendrycks and Gimpel, 2016).
+ *
+ *  silu_and_mul -- Megatron-LM PR "Size MoE activation kernel grid to the row
+ *      count", section "What changed and why": the elementwise MoE activation
+ *      out_j = silu(g_j) * u_j with silu(x) = x / (1 + exp(-x)), gate in the
+ *      first d columns and up in the next d.
+ *
+ * Inputs are bf16 bit patterns (uint16), decoded exactly to double.  The
+ * bf16 encoder below rounds a double to the nearest bf16, ties to even, in
+ * one step (no detour through float, which would round twice).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_PI 3.14159265358979323846
+
+/* Exact value of a bf16 bit pattern: the top 16 bits of an IEEE binary32. */
+double oracle_bf16_to_double(uint16_t bits)
+{
+    uint32_t w = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &w, sizeof f);
+    return (double)f;
+}
+
+/*
+ * Round a double to the nearest bf16 (8 significant bits, binary32 exponent
+ * range), ties to even, with gradual underflow and overflow to infinity.
+ * Method: pick the quantum 2^(e-7) of the binade of |v| (fixed at 2^-133
+ * below the smallest normal 2^-126), divide by it (exact: a power of two),
+ * round to the nearest integer with ties to even (rint in the default
+ * rounding mode), scale back.
+ */
+uint16_t oracle_double_to_bf16(double v)
+{
+    uint16_t sign = signbit(v) ? 0x8000u : 0u;
+    if (isnan(v))
+        return (uint16_t)(sign | 0x7FC0u);
+    double a = fabs(v);
+    if (a == 0.0)
+        return sign;
+    /* largest finite bf16 is (2 - 2^-7) 2^127; halfway to 2^128 rounds up */
+    if (isinf(a) || a >= ldexp(2.0 - ldexp(1.0, -8), 127))
+        return (uint16_t)(sign | 0x7F80u);
+    int e2;
+    frexp(a, &e2);            /* a = m 2^e2, m in [0.5, 1)  ->  binade 2^(e2-1) */
+    int e = e2 - 1;
+    if (e < -126)
+        e = -126;
+    double q = ldexp(1.0, e - 7);
+    double r = rint(a / q) * q;   /* exactly representable in binary32 */
+    float f = (float)r;
+    uint32_t w;
+    memcpy(&w, &f, sizeof w);
+    return (uint16_t)(sign | (uint16_t)(w >> 16));
+}
+
+/* tanh-approximate GELU, in double with libm tanh. */
+double oracle_gelu_tanh(double x)
+{
+    const double k = sqrt(2.0 / ORACLE_PI);
+    return 0.5 * x * (1.0 + tanh(k * (x + 0.044715 * x * x * x)));
+}
+
+/* SiLU (swish), in double with libm exp. */
+double oracle_silu(double x)
+{
+    return x / (1.0 + exp(-x));
+}
+
+static void set_threads(int nthreads)
+{
+#ifdef _OPENMP
+    if (nthreads > 0)
+        omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+}
+
+/* Number of threads an OpenMP region would use (1 without OpenMP). */
+int oracle_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/*
+ * gelu_and_mul_sparse, one row at a time.
+ *   in         : T rows of row_stride bf16 values; gate = [0,d), up = [d,2d)
+ *   ref        : T*d doubles, the unrounded result
+ *   mask       : T*d bytes, 1 where g_j > cutoff (strictly), else 0
+ *   row_mean, row_std, row_cutoff : T doubles each (any may be NULL)
+ *   nthreads   : OpenMP threads over rows (<= 0: the runtime default)
+ * Returns 0, or -1 on a bad size.
+ */
+int oracle_gelu_and_mul_sparse(const uint16_t *in, int64_t T, int64_t d,
+                               int64_t row_stride, double z, double *ref,
+                               uint8_t *mask, double *row_mean,
+                               double *row_std, double *row_cutoff,
+                               int nthreads)
+{
+    if (T < 0 || d <= 0 || row_stride < 2 * d)
+        return -1;
+    set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < T; ++r) {
+        const uint16_t *gate = in + r * row_stride;
+        const uint16_t *up = gate + d;
+
+        double sum = 0.0;
+        for (int64_t j = 0; j < d; ++j)
+            sum += oracle_bf16_to_double(gate[j]);
+        double mean = sum / (double)d;
+
+        double ss = 0.0;
+        for (int64_t j = 0; j < d; ++j) {
+            double dev = oracle_bf16_to_double(gate[j]) - mean;
+            ss += dev * dev;
+        }
+        double var = ss / (double)d;
+        double std = sqrt(var);
+
+        double cutoff = mean + std * z;
+
+        for (int64_t j = 0; j < d; ++j) {
+            double g = oracle_bf16_to_double(gate[j]);
+            double u = oracle_bf16_to_double(up[j]);
+            double s = g - cutoff;
+            if (s < 0.0)
+                s = 0.0;
+            ref[r * d + j] = oracle_gelu_tanh(s) * u;
+            if (mask)
+                mask[r * d + j] = (uint8_t)(g > cutoff);
+        }
+        if (row_mean)
+            row_mean[r] = mean;
+        if (row_std)
+            row_std[r] = std;
+        if (row_cutoff)
+            row_cutoff[r] = cutoff;
+    }
+    return 0;
+}
+
+/*
+ * silu_and_mul over a contiguous [M, 2d] bf16 input.
+ *   ref      : M*d doubles, silu(g) * u unrounded (may be NULL)
+ *   ref_bf16 : M*d bf16 bit patterns, ref rounded to nearest-even (may be NULL)
+ * Returns 0, or -1 on a bad size.
+ */
+int oracle_silu_and_mul(const uint16_t *in, int64_t M, int64_t d, double *ref,
+                        uint16_t *ref_bf16, int nthreads)
+{
+    if (M < 0 || d <= 0)
+        return -1;
+    set_threads(nthreads);
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < M; ++r) {
+        const uint16_t *gate = in + r * 2 * d;
+        const uint16_t *up = gate + d;
+        for (int64_t j = 0; j < d; ++j) {
+            double y = oracle_silu(oracle_bf16_to_double(gate[j])) *
+                       oracle_bf16_to_double(up[j]);
+            if (ref)
+                ref[r * d + j] = y;
+            if (ref_bf16)
+                ref_bf16[r * d + j] = oracle_double_to_bf16(y);
+        }
+    }
+    return 0;
+}
