@@ -1,0 +1,177 @@
+"""Python binding of the GB300 fused gated-activation library.
+
+Argument marshalling only: every step of both activations runs in the CUDA
+library ``_lib/libgated_act.so`` (built from ``csrc/`` by ``build.py``) behind
+the C ABI declared in ``include/gated_act.h``.  PyTorch supplies device memory
+and the current stream.  There is no CPU or eager fallback: if the library is
+missing or a call fails, this module raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+from . import build as _build
+
+LIB_PATH = _build.LIB
+
+OK = 0
+ERR_NULL, ERR_SIZE, ERR_STRIDE, ERR_TOO_LARGE = -1, -2, -3, -4
+ERR_OVERLAP, ERR_VARIANT, ERR_CUDA, ERR_ALIGN = -5, -6, -7, -8
+
+VARIANT_AUTO, VARIANT_WARP_ROWS, VARIANT_CTA_ROW, VARIANT_SCALAR = 0, 1, 2, 3
+VARIANT_NAMES = {0: "auto", 1: "warp_rows", 2: "cta_row", 3: "scalar"}
+
+EXPORTED = (
+    "gelu_and_mul_sparse", "silu_and_mul", "gated_act_status_string",
+    "gated_act_last_cuda_error", "gelu_and_mul_sparse_plan", "gelu_and_mul_sparse_ex",
+)
+
+
+class GatedActError(RuntimeError):
+    def __init__(self, fn: str, status: int, msg: str):
+        super().__init__(f"{fn}: status {status}: {msg}")
+        self.status = status
+
+
+class Plan(ctypes.Structure):
+    """Mirror of ``gated_act_plan``."""
+
+    _fields_ = [("variant", ctypes.c_int32), ("cluster", ctypes.c_int32),
+                ("threads", ctypes.c_int32), ("vec_per_thread", ctypes.c_int32),
+                ("rows_per_cta", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("grid", ctypes.c_int64)]
+
+    def as_dict(self) -> dict:
+        return {"variant": VARIANT_NAMES.get(self.variant, str(self.variant)),
+                "cluster": self.cluster, "threads": self.threads,
+                "vec_per_thread": self.vec_per_thread, "rows_per_cta": self.rows_per_cta,
+                "grid": self.grid}
+
+
+_lib: ctypes.CDLL | None = None
+
+
+def load_library(path: str | None = None) -> ctypes.CDLL:
+    """Load the CUDA library (once) and declare the C signatures."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise ImportError(
+            f"CUDA library {p} is missing: build it with "
+            "`python -c 'import __graft_entry__ as g; g.build()'` (no fallback exists)")
+    lib = ctypes.CDLL(p)
+    i64, vp, cvp = ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p
+    lib.gelu_and_mul_sparse.argtypes = [vp, cvp, i64, i64, i64, ctypes.c_double, vp]
+    lib.gelu_and_mul_sparse.restype = ctypes.c_int
+    lib.gelu_and_mul_sparse_ex.argtypes = [vp, cvp, i64, i64, i64, ctypes.c_double,
+                                           ctypes.c_int, ctypes.c_int, vp]
+    lib.gelu_and_mul_sparse_ex.restype = ctypes.c_int
+    lib.gelu_and_mul_sparse_plan.argtypes = [cvp, cvp, i64, i64, i64, ctypes.c_int,
+                                             ctypes.c_int, ctypes.c_int, ctypes.POINTER(Plan)]
+    lib.gelu_and_mul_sparse_plan.restype = ctypes.c_int
+    lib.silu_and_mul.argtypes = [vp, cvp, i64, i64, vp]
+    lib.silu_and_mul.restype = ctypes.c_int
+    lib.gated_act_status_string.argtypes = [ctypes.c_int]
+    lib.gated_act_status_string.restype = ctypes.c_char_p
+    lib.gated_act_last_cuda_error.argtypes = []
+    lib.gated_act_last_cuda_error.restype = ctypes.c_int
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load_library().gated_act_status_string(int(status)).decode()
+
+
+def _check(fn: str, rc: int) -> None:
+    if rc != OK:
+        msg = status_string(rc)
+        if rc == ERR_CUDA:
+            msg += f" (cudaError {load_library().gated_act_last_cuda_error()})"
+        raise GatedActError(fn, rc, msg)
+
+
+def _stream_handle(stream: torch.cuda.Stream | None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def _rows_view(x: torch.Tensor) -> tuple[int, int]:
+    """(T, row_stride) for a 2-D bf16 CUDA tensor whose rows may be strided."""
+    if x.dim() != 2:
+        raise ValueError("input must be 2-D [T, row_stride]")
+    if x.dtype != torch.bfloat16:
+        raise TypeError("input must be bfloat16")
+    if not x.is_cuda:
+        raise ValueError("input must be a CUDA tensor (the library has no CPU path)")
+    if x.stride(1) != 1:
+        raise ValueError("input columns must be contiguous")
+    return int(x.shape[0]), int(x.stride(0)) if x.shape[0] > 1 else int(x.shape[1])
+
+
+def gelu_and_mul_sparse(x: torch.Tensor, z: float, d: int | None = None,
+                        out: torch.Tensor | None = None, variant: int = VARIANT_AUTO,
+                        cluster: int = 0, stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """Sparse GELU gate of ``x`` ([T, >=2d] bf16 CUDA): returns ``out`` [T, d] bf16.
+
+    ``d`` defaults to half the row length.  Rows may be strided (x[:, :2d] of a
+    wider buffer).  ``variant``/``cluster`` force a launch geometry.
+    """
+    T, rs = _rows_view(x)
+    if d is None:
+        if x.shape[1] % 2:
+            raise ValueError("odd row length: pass d explicitly")
+        d = int(x.shape[1]) // 2
+    if x.shape[1] < 2 * d:
+        raise ValueError("rows are shorter than 2d")
+    if out is None:
+        out = torch.empty((T, d), dtype=torch.bfloat16, device=x.device)
+    elif out.shape != (T, d) or out.dtype != torch.bfloat16 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous [T, d] bf16 tensor")
+    lib = load_library()
+    rc = lib.gelu_and_mul_sparse_ex(out.data_ptr(), x.data_ptr(), T, d, rs, float(z),
+                                    int(variant), int(cluster), _stream_handle(stream))
+    _check("gelu_and_mul_sparse", rc)
+    return out
+
+
+def gelu_and_mul_sparse_plan(x: torch.Tensor, d: int | None = None, out: torch.Tensor | None = None,
+                             variant: int = VARIANT_AUTO, cluster: int = 0) -> dict:
+    """The launch geometry gelu_and_mul_sparse would use for this call."""
+    T, rs = _rows_view(x)
+    d = int(x.shape[1]) // 2 if d is None else d
+    p = Plan()
+    out_ptr = out.data_ptr() if out is not None else 0
+    rc = load_library().gelu_and_mul_sparse_plan(out_ptr, x.data_ptr(), T, d, rs,
+                                                 int(variant), int(cluster), 0, ctypes.byref(p))
+    _check("gelu_and_mul_sparse_plan", rc)
+    return p.as_dict()
+
+
+def silu_and_mul(x: torch.Tensor, out: torch.Tensor | None = None,
+                 stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """silu(gate) * up of a contiguous [M, 2d] bf16 CUDA tensor: returns [M, d] bf16."""
+    if x.dim() != 2 or x.dtype != torch.bfloat16 or not x.is_cuda or not x.is_contiguous():
+        raise ValueError("input must be a contiguous 2-D bf16 CUDA tensor [M, 2d]")
+    M, w = int(x.shape[0]), int(x.shape[1])
+    if w % 2:
+        raise ValueError("row length must be even (2d)")
+    d = w // 2
+    if out is None:
+        out = torch.empty((M, d), dtype=torch.bfloat16, device=x.device)
+    elif out.shape != (M, d) or out.dtype != torch.bfloat16 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous [M, d] bf16 tensor")
+    rc = load_library().silu_and_mul(out.data_ptr(), x.data_ptr(), M, d, _stream_handle(stream))
+    _check("silu_and_mul", rc)
+    return out
+
+
+__all__ = ["gelu_and_mul_sparse", "gelu_and_mul_sparse_plan", "silu_and_mul", "load_library",
+           "status_string", "GatedActError", "Plan", "EXPORTED", "LIB_PATH"]

@@ -1,0 +1,57 @@
+// Status strings, per-thread CUDA error record and cached device facts.
+#include <atomic>
+
+#include "common.cuh"
+
+namespace gact {
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sm_count[kMaxDevices];   // 0 = not queried yet
+
+}  // namespace
+
+int device_sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0)
+        return 1;
+    if (dev < kMaxDevices) {
+        const int cached = g_sm_count[dev].load(std::memory_order_relaxed);
+        if (cached > 0)
+            return cached;
+    }
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+        n = 1;
+    if (dev < kMaxDevices)
+        g_sm_count[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
+
+int cuda_status(cudaError_t e) {
+    if (e == cudaSuccess)
+        return GATED_ACT_OK;
+    g_last_cuda_error = static_cast<int>(e);
+    return GATED_ACT_ERR_CUDA;
+}
+
+}  // namespace gact
+
+extern "C" const char *gated_act_status_string(int status) {
+    switch (status) {
+    case GATED_ACT_OK: return "ok";
+    case GATED_ACT_ERR_NULL: return "null input or output pointer";
+    case GATED_ACT_ERR_SIZE: return "bad size: rows must be >= 0 and d >= 1";
+    case GATED_ACT_ERR_STRIDE: return "row_stride is smaller than 2*d";
+    case GATED_ACT_ERR_TOO_LARGE: return "problem too large for the index arithmetic";
+    case GATED_ACT_ERR_OVERLAP: return "output overlaps the input";
+    case GATED_ACT_ERR_VARIANT: return "requested launch geometry does not fit this call";
+    case GATED_ACT_ERR_CUDA: return "CUDA runtime error at launch (see gated_act_last_cuda_error)";
+    case GATED_ACT_ERR_ALIGN: return "pointer is not 2-byte aligned";
+    default: return "unknown status";
+    }
+}
+
+extern "C" int gated_act_last_cuda_error(void) { return gact::g_last_cuda_error; }

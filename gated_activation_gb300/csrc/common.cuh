@@ -1,0 +1,76 @@
+// Internal helpers shared by the library's translation units (device side
+// bf16 packing, streaming loads, warp reductions; host side argument checks
+// and device facts).  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "gated_act.h"
+
+namespace gact {
+
+// ---------------------------------------------------------------- device side
+
+// 8 bf16 values = one 16-byte vector, kept packed as four bf16x2 words.
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Round two floats to bf16 (nearest even) and pack them, lo in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// 16-byte load of data that is read once: read-only path, no L1 allocation.
+__device__ __forceinline__ uint4 ld_stream(const void *p) {
+    uint4 r;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ uint16_t ld_stream_u16(const uint16_t *p) {
+    uint16_t r;
+    asm("ld.global.nc.u16 %0, [%1];" : "=h"(r) : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ void st_vec(void *p, uint4 v) {
+    asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};"
+                 :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+// Butterfly sum: every lane ends with the same bits (fp add is commutative
+// and each step pairs the same two operands in both partner lanes).
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+
+// ---------------------------------------------------------------- host side
+
+// Per-device facts, queried once per device and cached.
+int device_sm_count();
+
+// Record a CUDA error for gated_act_last_cuda_error() and map it to a status.
+int cuda_status(cudaError_t e);
+
+inline bool aligned(const void *p, uintptr_t a) {
+    return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
+}
+
+// True when [a, a + na) and [b, b + nb) (byte ranges) intersect.
+inline bool ranges_overlap(const void *a, uint64_t na, const void *b, uint64_t nb) {
+    uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    if (na == 0 || nb == 0)
+        return false;
+    return x < y + nb && y < x + na;
+}
+
+}  // namespace gact

@@ -1,0 +1,132 @@
+// silu_and_mul for sm_103a: out = silu(gate) * up over [M, 2d] bf16 rows.
+//
+// Megatron-LM PR "Size MoE activation kernel grid to the row count",
+// sections "What changed and why" and "Correctness": a pure elementwise op
+// whose cost is launch geometry.  Here the grid is sized to the work -- every
+// thread owns kVecPerThread 16-byte output vectors spread over the whole
+// [M, d] output (consecutive threads take consecutive vectors, so every warp
+// access is one contiguous 512-byte run) -- and all loads are issued before
+// any math.  Per element the math is fp32 and independent of the geometry,
+// so any grid gives the same bits.
+#include <algorithm>
+
+#include "common.cuh"
+
+namespace gact {
+namespace {
+
+constexpr int kSiluThreads = 256;
+constexpr int kVecPerThread = 2;
+
+// silu(g) * u in fp32 as g * sigmoid(g), with the sigmoid taken from
+// t = e^-|g| (never overflows): 1 / (1 + t) for g >= 0, t / (1 + t) below.
+// The naive 1 / (1 + e^-g) overflows for g < -88.7 and returns -0 where the
+// true product is still a normal bf16 number.
+// e^x = 2^(x log2 e) on the hardware base-2 exponential (PTX ISA ex2.approx.f32,
+// the non-flushing form: subnormal results survive, which keeps silu(g) for
+// g in (-104, -87] a normal bf16 number instead of -0).
+__device__ __forceinline__ float exp_neg_abs(float g) {
+    const float x = -fabsf(g) * 1.4426950408889634f;
+    float y;
+    asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u) {
+    const float t = exp_neg_abs(g);
+    const float r = __frcp_rn(1.0f + t);
+    return g * (g >= 0.f ? r : t * r) * u;
+}
+
+__device__ __forceinline__ uint32_t silu2(uint32_t g, uint32_t u) {
+    return pack_bf16x2(silu_mul(bf16_lo(g), bf16_lo(u)), silu_mul(bf16_hi(g), bf16_hi(u)));
+}
+
+// Idx = uint32_t when M * d / 8 < 2^32 (cheap division), else uint64_t.
+template <typename Idx>
+__global__ void __launch_bounds__(kSiluThreads)
+silu_vec(uint16_t *__restrict__ out, const uint16_t *__restrict__ in, Idx total, Idx nv,
+         int64_t d) {
+    const Idx nthreads = static_cast<Idx>(gridDim.x) * kSiluThreads;
+    const Idx first = static_cast<Idx>(blockIdx.x) * kSiluThreads + threadIdx.x;
+    for (Idx base = first; base < total; base += nthreads * kVecPerThread) {
+        uint4 g[kVecPerThread], u[kVecPerThread];
+        Idx idx[kVecPerThread];
+#pragma unroll
+        for (int i = 0; i < kVecPerThread; ++i) {
+            idx[i] = base + nthreads * i;
+            if (idx[i] < total) {
+                const Idx r = idx[i] / nv, c = idx[i] - r * nv;
+                const uint16_t *gp = in + static_cast<int64_t>(r) * 2 * d + 8 * static_cast<int64_t>(c);
+                g[i] = ld_stream(gp);
+                u[i] = ld_stream(gp + d);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kVecPerThread; ++i) {
+            if (idx[i] < total) {
+                const Idx r = idx[i] / nv, c = idx[i] - r * nv;
+                const uint4 o = make_uint4(silu2(g[i].x, u[i].x), silu2(g[i].y, u[i].y),
+                                           silu2(g[i].z, u[i].z), silu2(g[i].w, u[i].w));
+                st_vec(out + static_cast<int64_t>(r) * d + 8 * static_cast<int64_t>(c), o);
+            }
+        }
+    }
+}
+
+// Any layout: one element per thread iteration, 2-byte accesses.
+__global__ void __launch_bounds__(kSiluThreads)
+silu_scalar(uint16_t *__restrict__ out, const uint16_t *__restrict__ in, int64_t M, int64_t d) {
+    const int64_t total = M * d;
+    const int64_t step = static_cast<int64_t>(gridDim.x) * kSiluThreads;
+    for (int64_t e = static_cast<int64_t>(blockIdx.x) * kSiluThreads + threadIdx.x; e < total;
+         e += step) {
+        const int64_t r = e / d, c = e - r * d;
+        const uint16_t *gp = in + r * 2 * d + c;
+        const float g = __uint_as_float(static_cast<uint32_t>(ld_stream_u16(gp)) << 16);
+        const float u = __uint_as_float(static_cast<uint32_t>(ld_stream_u16(gp + d)) << 16);
+        out[e] = __bfloat16_as_ushort(__float2bfloat16_rn(silu_mul(g, u)));
+    }
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+}  // namespace
+}  // namespace gact
+
+extern "C" int silu_and_mul(void *out, const void *in, int64_t M, int64_t d,
+                            cudaStream_t stream) {
+    using namespace gact;
+    if (M < 0 || d <= 0)
+        return GATED_ACT_ERR_SIZE;
+    if (d > (int64_t(1) << 30) || M > (int64_t(1) << 40))
+        return GATED_ACT_ERR_TOO_LARGE;
+    if (M == 0)
+        return GATED_ACT_OK;
+    if (!out || !in)
+        return GATED_ACT_ERR_NULL;
+    if (!aligned(out, 2) || !aligned(in, 2))
+        return GATED_ACT_ERR_ALIGN;
+    const uint64_t out_bytes = 2ull * static_cast<uint64_t>(M * d);
+    if (ranges_overlap(out, out_bytes, in, 2 * out_bytes))
+        return GATED_ACT_ERR_OVERLAP;
+
+    uint16_t *o = static_cast<uint16_t *>(out);
+    const uint16_t *x = static_cast<const uint16_t *>(in);
+    const bool vec_ok = aligned(in, 16) && aligned(out, 16) && d % 8 == 0;
+    if (vec_ok) {
+        const int64_t nv = d / 8, total = M * nv;
+        const int64_t grid = std::min<int64_t>(
+            ceil_div(ceil_div(total, kVecPerThread), kSiluThreads), 0x7FFFFFFF);
+        if (total < (int64_t(1) << 32) - int64_t(grid) * kSiluThreads * kVecPerThread)
+            silu_vec<uint32_t><<<static_cast<unsigned>(grid), kSiluThreads, 0, stream>>>(
+                o, x, static_cast<uint32_t>(total), static_cast<uint32_t>(nv), d);
+        else
+            silu_vec<uint64_t><<<static_cast<unsigned>(grid), kSiluThreads, 0, stream>>>(
+                o, x, static_cast<uint64_t>(total), static_cast<uint64_t>(nv), d);
+    } else {
+        const int64_t grid = std::min<int64_t>(ceil_div(M * d, kSiluThreads), int64_t(1) << 20);
+        silu_scalar<<<static_cast<unsigned>(grid), kSiluThreads, 0, stream>>>(o, x, M, d);
+    }
+    return cuda_status(cudaGetLastError());
+}

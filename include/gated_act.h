@@ -1,0 +1,153 @@
+/*
+ * gated_act.h -- C ABI of the GB300 (sm_103a) fused gated-activation library.
+ *
+ * Two operations over bf16 activations, each one kernel launch:
+ *
+ *   gelu_and_mul_sparse  Gemma3n's sparse GELU gate.  vLLM PR "[Performance]
+ *       Add Triton kernel for Gemma3n sparse GELU", section "Purpose": per-row
+ *       mean and variance, Gaussian thresholding, tanh GELU and the gated
+ *       multiplication, fused.  For each row with gate g = columns [0, d) and
+ *       up u = columns [d, 2d):
+ *           mean   = sum_j g_j / d                    (fp32 accumulation)
+ *           std    = sqrt(sum_j (g_j - mean)^2 / d)   (population std)
+ *           cutoff = mean + std * z,   z = inverse normal CDF of the target
+ *                                      sparsity (0.95 -> 1.6448536269514722)
+ *           out_j  = gelu_tanh(max(g_j - cutoff, 0)) * u_j
+ *           gelu_tanh(x) = 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3)))
+ *       computed in fp32 and rounded once to bf16 (nearest even).
+ *
+ *   silu_and_mul  the MoE expert activation of Megatron-LM PR "Size MoE
+ *       activation kernel grid to the row count", section "What changed and
+ *       why": out_j = silu(g_j) * u_j, silu(x) = x / (1 + exp(-x)), fp32 math,
+ *       bf16 out.
+ *
+ * Conventions shared by every entry point
+ *   - bf16 means 2-byte IEEE bfloat16 storage; all pointers are DEVICE
+ *     pointers of the current CUDA device, owned by the caller.  The library
+ *     allocates nothing, keeps no state between calls, never synchronizes the
+ *     host and launches only on `stream` (0 = the legacy default stream), so
+ *     every call is asynchronous and can be captured in a CUDA graph.
+ *   - The launch geometry depends only on the arguments, the pointers'
+ *     alignment and the device's SM count.
+ *   - 16-byte vector paths are taken when `in`, `out`, the row stride and d
+ *     allow 16-byte aligned rows (pointers 16-byte aligned, row_stride and d
+ *     multiples of 8); any other layout runs the scalar path -- slower, same
+ *     results -- never an error.
+ *   - Return value: GATED_ACT_OK (0) or a negative gated_act_status.  A
+ *     negative value other than GATED_ACT_ERR_CUDA means nothing was launched.
+ *     A zero-row call (T == 0 or M == 0) launches nothing and returns 0.
+ *   - NaN/Inf follow IEEE arithmetic: a NaN anywhere in a gate row makes that
+ *     whole output row NaN (it reaches the mean); a NaN in up stays in its
+ *     element.
+ */
+#ifndef GATED_ACT_H
+#define GATED_ACT_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gated_act_status {
+    GATED_ACT_OK = 0,
+    GATED_ACT_ERR_NULL = -1,       /* null in/out with a non-empty problem       */
+    GATED_ACT_ERR_SIZE = -2,       /* T or M < 0, or d <= 0                      */
+    GATED_ACT_ERR_STRIDE = -3,     /* row_stride < 2 d                           */
+    GATED_ACT_ERR_TOO_LARGE = -4,  /* d > 2^30 or a byte range overflows int64   */
+    GATED_ACT_ERR_OVERLAP = -5,    /* the bytes out writes overlap the bytes in reads */
+    GATED_ACT_ERR_VARIANT = -6,    /* a forced variant/cluster size does not fit the call */
+    GATED_ACT_ERR_CUDA = -7,       /* the CUDA runtime reported an error at launch */
+    GATED_ACT_ERR_ALIGN = -8       /* a pointer is not 2-byte aligned            */
+} gated_act_status;
+
+/*
+ * gelu_and_mul_sparse -- fused sparse GELU gate (definition above).
+ *   out        [T, d] bf16, contiguous (row r at out + r*d).  Written only.
+ *   in         [T, row_stride] bf16; row r: gate = in[r*row_stride + j],
+ *              up = in[r*row_stride + d + j], j in [0, d).  Columns past 2d
+ *              are never read.  Read only; must not overlap out.
+ *   T          rows, >= 0.       d  gate/up width, >= 1.
+ *   row_stride elements between consecutive input rows, >= 2d.
+ *   z          threshold in standard deviations (applied in fp32).
+ *   stream     CUDA stream to launch on.
+ * Accuracy (against an fp64 evaluation of the definition): every element
+ * within 1e-2 |ref| + 2e-3; the zero pattern equals {g > cutoff} except where
+ * |g - cutoff| < 1e-3 std.  A row whose gate is constant gives exact zeros
+ * for d <= 65536 (its fp32 sum is exact).
+ */
+int gelu_and_mul_sparse(void *out, const void *in, int64_t T, int64_t d,
+                        int64_t row_stride, double z, cudaStream_t stream);
+
+/*
+ * silu_and_mul -- out = silu(gate) * up, elementwise.
+ *   out  [M, d] bf16 contiguous, written only.
+ *   in   [M, 2d] bf16 contiguous: gate = columns [0, d), up = [d, 2d).
+ *   M    rows, >= 0.   d >= 1.
+ * Accuracy: within one bf16 ulp of the correctly rounded result.
+ */
+int silu_and_mul(void *out, const void *in, int64_t M, int64_t d,
+                 cudaStream_t stream);
+
+/* Human-readable text for a status code (static storage; never NULL). */
+const char *gated_act_status_string(int status);
+
+/* The cudaError_t behind the calling thread's last GATED_ACT_ERR_CUDA (0 if none). */
+int gated_act_last_cuda_error(void);
+
+/* ------------------------------------------------------------------------
+ * Launch-geometry control, for tests and measurements.
+ *
+ * gelu_and_mul_sparse picks one of these geometries; the choice never changes
+ * the definition, only the fp32 summation order (results agree within the
+ * accuracy bound above; rows with the same geometry agree bitwise).
+ * ------------------------------------------------------------------------ */
+typedef enum gated_act_variant {
+    GATED_ACT_VARIANT_AUTO = 0,      /* the library's own choice                   */
+    GATED_ACT_VARIANT_WARP_ROWS = 1, /* one warp per row, several rows per CTA     */
+    GATED_ACT_VARIANT_CTA_ROW = 2,   /* one CTA, or a cluster of CTAs, per row;
+                                        row held in registers                       */
+    GATED_ACT_VARIANT_SCALAR = 3     /* any layout: one CTA per row, 2-byte loads   */
+} gated_act_variant;
+
+typedef struct gated_act_plan {
+    int32_t variant;        /* gated_act_variant actually used                */
+    int32_t cluster;        /* CTAs that share one row (1 = none)             */
+    int32_t threads;        /* threads per CTA                                 */
+    int32_t vec_per_thread; /* 16-byte vectors of gate per thread (0: scalar)  */
+    int32_t rows_per_cta;   /* rows one CTA handles at a time                  */
+    int32_t reserved;
+    int64_t grid;           /* CTAs launched                                   */
+} gated_act_plan;
+
+/*
+ * Describe the launch gelu_and_mul_sparse(_ex) would make, without launching.
+ * variant/cluster as in gelu_and_mul_sparse_ex; out/in are only inspected for
+ * alignment (never dereferenced).  sm_count > 0 plans for a device with that
+ * many SMs; sm_count <= 0 queries the current device (its only CUDA call).
+ * Returns 0 and fills *plan, or a negative status (GATED_ACT_ERR_VARIANT when
+ * the forced geometry does not fit).
+ */
+int gelu_and_mul_sparse_plan(const void *out, const void *in, int64_t T,
+                             int64_t d, int64_t row_stride, int variant,
+                             int cluster, int sm_count, gated_act_plan *plan);
+
+/*
+ * gelu_and_mul_sparse with a forced geometry.
+ *   variant  a gated_act_variant; AUTO behaves like gelu_and_mul_sparse.
+ *   cluster  for GATED_ACT_VARIANT_CTA_ROW: CTAs per row, a power of two
+ *            in [1, 8], or 0 to let the library choose; ignored otherwise.
+ * Returns GATED_ACT_ERR_VARIANT when the layout cannot use that geometry
+ * (vector variants need the 16-byte layout above; a row slice must fit the
+ * CTA's registers).
+ */
+int gelu_and_mul_sparse_ex(void *out, const void *in, int64_t T, int64_t d,
+                           int64_t row_stride, double z, int variant,
+                           int cluster, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GATED_ACT_H */

@@ -1,0 +1,97 @@
+"""Acceptance checks of CUDA outputs against the fp64 oracle (test helper).
+
+gelu_and_mul_sparse, per element (ref = oracle's unrounded fp64 value):
+  * |out - ref| <= 1e-2 |ref| + 2e-3;
+  * the zero pattern: out != 0 exactly where g > cutoff (and the product is
+    not zero), except inside the flip band |g - cutoff| < 1e-3 std, where
+    either outcome is correct: out == 0, or the small value that the kernel's
+    own fp32 cutoff gives, bounded by gelu(s) <= s with s < 2e-3 std;
+  * NaN exactly where the oracle has NaN.
+Rows with std == 0 have an empty band, so their zero pattern must match
+exactly.
+
+silu_and_mul: the bf16 output is within one ulp of the oracle's correctly
+rounded bf16, the distance taken on the ordered integer line of bf16
+patterns (+0 and -0 equal).
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+RTOL, ATOL, BAND = 1e-2, 2e-3, 1e-3
+
+
+def bits_of(t: torch.Tensor) -> np.ndarray:
+    t = t.detach().to("cpu").contiguous()
+    assert t.dtype == torch.bfloat16
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def f64_of_bits(bits: np.ndarray) -> np.ndarray:
+    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def check_gelu(out: torch.Tensor, x: torch.Tensor, d: int, res, label: str = "") -> dict:
+    """Assert the acceptance criteria; return summary statistics."""
+    y = f64_of_bits(bits_of(out))
+    xb = bits_of(x)
+    g = f64_of_bits(xb[:, :d])
+    u = f64_of_bits(xb[:, d:2 * d])
+    ref = res.ref
+    assert y.shape == ref.shape, (label, y.shape, ref.shape)
+    cutoff = res.cutoff[:, None]
+    std = res.std[:, None]
+
+    nan_ref = np.isnan(ref)
+    nan_y = np.isnan(y)
+    assert np.array_equal(nan_ref, nan_y), f"{label}: NaN pattern differs ({(nan_ref != nan_y).sum()} elements)"
+    fin = ~nan_ref
+
+    with np.errstate(invalid="ignore"):
+        err = np.abs(y - ref)
+        tol = RTOL * np.abs(ref) + ATOL
+        band = np.abs(g - cutoff) < BAND * std
+        ok_val = err <= tol
+        flip_bound = (2 * BAND * std) * np.abs(u) * 1.01 + ATOL
+        ok_band = band & ((y == 0) | (np.abs(y) <= flip_bound) | ok_val)
+        bad = fin & ~(ok_val | ok_band)
+    if bad.any():
+        r, c = np.argwhere(bad)[0]
+        raise AssertionError(
+            f"{label}: {bad.sum()} elements out of tolerance; first at ({r},{c}): "
+            f"out={y[r, c]!r} ref={ref[r, c]!r} g={g[r, c]!r} u={u[r, c]!r} "
+            f"cutoff={res.cutoff[r]!r} std={res.std[r]!r}")
+
+    expect_nz = res.mask & (np.abs(ref) >= 2.0 ** -134)
+    mism = fin & ~band & ((y != 0) != expect_nz)
+    if mism.any():
+        r, c = np.argwhere(mism)[0]
+        raise AssertionError(
+            f"{label}: {mism.sum()} zero-mask mismatches outside the flip band; first at "
+            f"({r},{c}): out={y[r, c]!r} ref={ref[r, c]!r} g={g[r, c]!r} cutoff={res.cutoff[r]!r}")
+    flips = int((fin & band & ((y != 0) != expect_nz)).sum())
+    rel = np.where(fin & (np.abs(ref) > 1e-3), err / np.maximum(np.abs(ref), 1e-300), 0.0)
+    return {"max_abs_err": float(np.nanmax(np.where(fin, err, 0.0))) if y.size else 0.0,
+            "max_rel_err": float(rel.max()) if y.size else 0.0,
+            "band_flips": flips, "zero_fraction": float((y == 0).mean()) if y.size else 0.0}
+
+
+def ordered(bits: np.ndarray) -> np.ndarray:
+    """bf16 patterns -> integers ordered like the values (+0 and -0 both 0)."""
+    b = bits.astype(np.int64)
+    mag = b & 0x7FFF
+    return np.where(b & 0x8000, -mag, mag)
+
+
+def check_silu(out: torch.Tensor, ref16: np.ndarray, label: str = "") -> int:
+    """Assert <= 1 bf16 ulp from the correctly rounded oracle; return the max distance."""
+    ob = bits_of(out)
+    assert ob.shape == ref16.shape
+    nan_o = (ob & 0x7FFF) > 0x7F80
+    nan_r = (ref16 & 0x7FFF) > 0x7F80
+    assert np.array_equal(nan_o, nan_r), f"{label}: NaN pattern differs"
+    dist = np.abs(ordered(ob) - ordered(ref16))[~nan_r]
+    mx = int(dist.max()) if dist.size else 0
+    assert mx <= 1, f"{label}: {int((dist > 1).sum())} elements more than 1 ulp away (max {mx})"
+    return mx

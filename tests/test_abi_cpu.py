@@ -1,0 +1,162 @@
+"""The C-ABI library loads, exports every declared symbol, and its host-side
+logic (argument checks, status codes, launch-geometry planning) behaves --
+all without a GPU.  No call here launches a kernel: every call either fails
+validation before any CUDA call or is a plan query with an explicit SM count.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import gated_activation_gb300 as ga
+from gated_activation_gb300 import build as gbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gated_act.h")
+GB300_SMS = 152
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not gbuild.up_to_date():
+        gbuild.build()
+    return ga.load_library()
+
+
+def declared_functions() -> list[str]:
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    fns = declared_functions()
+    for name in ("gelu_and_mul_sparse", "silu_and_mul", "gated_act_status_string",
+                 "gelu_and_mul_sparse_ex", "gelu_and_mul_sparse_plan",
+                 "gated_act_last_cuda_error"):
+        assert name in fns
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in gated_act.h but not exported"
+    assert set(declared_functions()) == set(ga.EXPORTED)
+
+
+def test_status_strings(lib):
+    for code in range(-8, 1):
+        s = lib.gated_act_status_string(code)
+        assert s and s.decode()
+    assert lib.gated_act_status_string(-99).decode() == "unknown status"
+    assert lib.gated_act_last_cuda_error() == 0
+
+
+def _gelu(lib, out, inp, T, d, rs, z=1.0):
+    return lib.gelu_and_mul_sparse(out, inp, T, d, rs, z, None)
+
+
+@pytest.mark.parametrize("T,d,rs,code", [
+    (-1, 8, 16, ga.ERR_SIZE), (4, 0, 16, ga.ERR_SIZE), (4, -3, 16, ga.ERR_SIZE),
+    (4, 8, 15, ga.ERR_STRIDE), (4, 8, 0, ga.ERR_STRIDE),
+    (4, (1 << 30) + 8, 1 << 32, ga.ERR_TOO_LARGE),
+])
+def test_gelu_rejects_bad_sizes(lib, T, d, rs, code):
+    assert _gelu(lib, 0x1000, 0x100000, T, d, rs) == code
+
+
+def test_gelu_rejects_null_odd_and_overlapping_pointers(lib):
+    assert _gelu(lib, None, 0x100000, 4, 8, 16) == ga.ERR_NULL
+    assert _gelu(lib, 0x1000, None, 4, 8, 16) == ga.ERR_NULL
+    assert _gelu(lib, 0x1001, 0x100000, 4, 8, 16) == ga.ERR_ALIGN
+    assert _gelu(lib, 0x1000, 0x100001, 4, 8, 16) == ga.ERR_ALIGN
+    # in spans [0x10000, 0x10000 + 2*(3*16+16)) = 128 B; out [.., +64 B)
+    assert _gelu(lib, 0x10000 + 64, 0x10000, 4, 8, 16) == ga.ERR_OVERLAP
+    assert _gelu(lib, 0x10000 - 63, 0x10000, 4, 8, 16) == ga.ERR_ALIGN
+    assert _gelu(lib, 0x10000 - 62, 0x10000, 4, 8, 16) == ga.ERR_OVERLAP
+
+
+def test_zero_rows_is_a_no_op(lib):
+    assert _gelu(lib, None, None, 0, 8, 16) == ga.OK
+    assert lib.silu_and_mul(None, None, 0, 8, None) == ga.OK
+
+
+@pytest.mark.parametrize("M,d,code", [(-1, 8, ga.ERR_SIZE), (4, 0, ga.ERR_SIZE),
+                                      (4, (1 << 30) + 1, ga.ERR_TOO_LARGE)])
+def test_silu_rejects_bad_sizes(lib, M, d, code):
+    assert lib.silu_and_mul(0x1000, 0x100000, M, d, None) == code
+
+
+def test_silu_rejects_null_odd_and_overlap(lib):
+    assert lib.silu_and_mul(None, 0x100000, 4, 8, None) == ga.ERR_NULL
+    assert lib.silu_and_mul(0x1001, 0x100000, 4, 8, None) == ga.ERR_ALIGN
+    assert lib.silu_and_mul(0x100000 + 100, 0x100000, 4, 8, None) == ga.ERR_OVERLAP
+
+
+def plan(lib, T, d, rs=None, variant=0, cluster=0, sms=GB300_SMS, out=0x10000, inp=0x100000):
+    p = ga.Plan()
+    rc = lib.gelu_and_mul_sparse_plan(out, inp, T, d, rs or 2 * d, variant, cluster, sms,
+                                      ctypes.byref(p))
+    return rc, p.as_dict()
+
+
+def test_plan_geometry_families(lib):
+    # small d: a warp per row
+    rc, p = plan(lib, 2048, 2048)
+    assert rc == 0 and p["variant"] == "warp_rows" and p["vec_per_thread"] == 8
+    # large T, d = 16384: one CTA per row, whole grid of rows
+    rc, p = plan(lib, 2048, 16384)
+    assert rc == 0 and p["variant"] == "cta_row" and p["cluster"] == 1 and p["grid"] == 2048
+    # d = 32768 is split across a 2-CTA cluster even at large T
+    rc, p = plan(lib, 2048, 32768)
+    assert rc == 0 and p["cluster"] == 2 and p["grid"] == 4096
+    # small T: rows split across clusters so more SMs take part
+    rc, p = plan(lib, 1, 32768)
+    assert rc == 0 and p["cluster"] == 8
+    rc, p = plan(lib, 64, 8192)
+    assert rc == 0 and p["cluster"] * 64 >= GB300_SMS
+
+
+def test_plan_covers_every_slice(lib):
+    # threads x vectors of each CTA slice cover the row for every aligned d
+    for d in list(range(8, 4096, 8)) + [8192, 8200, 16384, 16392, 32768, 65536, 131072, 262144]:
+        for T in (1, 8, 64, 2048):
+            rc, p = plan(lib, T, d)
+            assert rc == 0
+            nvec = d // 8
+            if p["variant"] == "warp_rows":
+                assert 32 * p["vec_per_thread"] >= nvec
+            elif p["variant"] == "cta_row":
+                sv = -(-nvec // p["cluster"])
+                assert p["threads"] * p["vec_per_thread"] >= sv
+                assert p["threads"] <= 1024 and p["cluster"] <= 8
+                assert p["grid"] % p["cluster"] == 0
+            else:
+                pytest.fail(f"aligned d={d} fell back to scalar")
+
+
+def test_plan_falls_back_to_scalar(lib):
+    assert plan(lib, 4, 31)[1]["variant"] == "scalar"            # d not a multiple of 8
+    assert plan(lib, 4, 64, rs=130)[1]["variant"] == "scalar"    # row stride not 16-byte
+    assert plan(lib, 4, 64, inp=0x100002)[1]["variant"] == "scalar"   # misaligned pointer
+    assert plan(lib, 4, 262144 + 8)[1]["variant"] == "scalar"    # wider than 8 CTAs hold
+
+
+def test_plan_forced_variants(lib):
+    assert plan(lib, 4, 2048, variant=ga.VARIANT_CTA_ROW, cluster=2)[1]["cluster"] == 2
+    assert plan(lib, 4, 4096, variant=ga.VARIANT_WARP_ROWS)[0] == ga.ERR_VARIANT
+    assert plan(lib, 4, 64, variant=ga.VARIANT_CTA_ROW, cluster=3)[0] == ga.ERR_VARIANT
+    assert plan(lib, 4, 64, variant=ga.VARIANT_CTA_ROW, cluster=16)[0] == ga.ERR_VARIANT
+    assert plan(lib, 4, 65536, variant=ga.VARIANT_CTA_ROW, cluster=1)[0] == ga.ERR_VARIANT
+    assert plan(lib, 4, 31, variant=ga.VARIANT_WARP_ROWS)[0] == ga.ERR_VARIANT
+    assert plan(lib, 4, 64, variant=9)[0] == ga.ERR_VARIANT
+    assert plan(lib, 4, 64, variant=ga.VARIANT_SCALAR)[1]["variant"] == "scalar"
+
+
+def test_plan_depends_only_on_arguments(lib):
+    a = plan(lib, 64, 8192)
+    b = plan(lib, 64, 8192)
+    assert a == b
+    # a different SM count may change the split, never the validity
+    rc, p = plan(lib, 64, 8192, sms=32)
+    assert rc == 0 and p["cluster"] == 1

@@ -1,0 +1,207 @@
+"""GPU parity of gelu_and_mul_sparse against the fp64 oracle, through the C ABI.
+
+Every config of the workload set (tiny, decode, prefill, the T x d x z sweep
+with constant rows), every launch geometry, and the edge cases: empty, d=1,
+ragged widths, strided and misaligned rows, NaN, maximum on-chip widths,
+guard-band canaries and CUDA-graph capture.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from tests.gpu_util import guarded_empty, guards_intact, require_gpu
+from tests.parity import bits_of, check_gelu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ga():
+    return require_gpu()
+
+
+def run(ga, x_cpu, d, z, **kw):
+    x = x_cpu.to("cuda")
+    out = ga.gelu_and_mul_sparse(x, z, d=d, **kw)
+    torch.cuda.synchronize()
+    return out.cpu()
+
+
+def oracle_of(oracle, x_cpu, d, z):
+    return oracle.gelu_and_mul_sparse(W.to_bits(x_cpu.contiguous()), d=d, z=z)
+
+
+GEOMETRIES = [(0, 0), (1, 0), (2, 1), (2, 2), (2, 4), (2, 8), (3, 0)]
+
+
+@pytest.mark.parametrize("variant,cluster", GEOMETRIES)
+def test_tiny_every_geometry(ga, oracle, variant, cluster):
+    inp = W.tiny()
+    res = oracle_of(oracle, inp.x, inp.d, inp.z)
+    out = run(ga, inp.x, inp.d, inp.z, variant=variant, cluster=cluster)
+    check_gelu(out, inp.x, inp.d, res, f"tiny v{variant} c{cluster}")
+
+
+@pytest.mark.parametrize("T", W.DECODE_T)
+def test_decode(ga, oracle, T):
+    inp = W.decode(T)
+    res = oracle_of(oracle, inp.x, inp.d, inp.z)
+    out = run(ga, inp.x, inp.d, inp.z)
+    check_gelu(out, inp.x, inp.d, res, inp.name)
+
+
+@pytest.mark.parametrize("cluster", [1, 2, 4, 8])
+def test_decode_forced_clusters(ga, oracle, cluster):
+    inp = W.decode(16)
+    res = oracle_of(oracle, inp.x, inp.d, inp.z)
+    out = run(ga, inp.x, inp.d, inp.z, variant=2, cluster=cluster)
+    check_gelu(out, inp.x, inp.d, res, f"decode16 c{cluster}")
+
+
+def test_prefill_full(ga, oracle):
+    inp = W.prefill()
+    res = oracle_of(oracle, inp.x, inp.d, inp.z)
+    out = run(ga, inp.x, inp.d, inp.z)
+    stats = check_gelu(out, inp.x, inp.d, res, "prefill")
+    assert abs(stats["zero_fraction"] - 0.95) < 0.003
+
+
+@pytest.mark.parametrize("z", W.SWEEP_Z)
+@pytest.mark.parametrize("d", W.SWEEP_D)
+@pytest.mark.parametrize("T", W.SWEEP_T)
+def test_sweep(ga, oracle, T, d, z):
+    inp = W.sweep(T, d, z=z, const_rows=True)
+    res = oracle_of(oracle, inp.x, inp.d, z)
+    out = run(ga, inp.x, inp.d, z)
+    check_gelu(out, inp.x, inp.d, res, f"{inp.name} z={z}")
+    # the three constant-gate rows: std == 0, exact zeros
+    tail = out[-len(W.CONST_GATES):].to(torch.float32)
+    assert torch.count_nonzero(tail).item() == 0
+
+
+@pytest.mark.parametrize("cluster", [1, 2, 4, 8])
+@pytest.mark.parametrize("T,d", [(8, 8192), (64, 16384), (3, 32768)])
+def test_sweep_shapes_every_cluster(ga, oracle, T, d, cluster):
+    inp = W.sweep(T, d, const_rows=True)
+    res = oracle_of(oracle, inp.x, d, inp.z)
+    if (d // 8 + cluster - 1) // cluster > 4096:
+        pytest.skip("slice does not fit one CTA")
+    out = run(ga, inp.x, d, inp.z, variant=2, cluster=cluster)
+    check_gelu(out, inp.x, d, res, f"{inp.name} c{cluster}")
+
+
+def test_same_geometry_is_bitwise_deterministic(ga):
+    inp = W.sweep(64, 8192, const_rows=False)
+    x = inp.x.cuda()
+    a = ga.gelu_and_mul_sparse(x, inp.z)
+    b = ga.gelu_and_mul_sparse(x, inp.z)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+@pytest.mark.parametrize("T,d", [(1, 1), (5, 1), (3, 2), (4, 7), (9, 8), (5, 16), (3, 24), (7, 31),
+                                 (4, 33), (6, 128), (2, 255), (3, 2056), (2, 4104), (2, 16392),
+                                 (37, 1000), (2, 32776)])
+def test_ragged_widths(ga, oracle, T, d):
+    inp = W.iid(T, d, seed=T * 1009 + d)
+    res = oracle_of(oracle, inp.x, d, inp.z)
+    out = run(ga, inp.x, d, inp.z)
+    check_gelu(out, inp.x, d, res, f"T{T} d{d}")
+    if d == 1:
+        assert torch.count_nonzero(out.float()).item() == 0
+
+
+@pytest.mark.parametrize("d,extra", [(64, 8), (2048, 16), (8192, 8), (1000, 24), (64, 3), (2048, 1)])
+def test_strided_rows_never_read_padding(ga, oracle, d, extra):
+    # padding columns hold NaN: any read of them would poison the row
+    inp = W.iid(11, d, seed=d + extra, row_stride=2 * d + extra)
+    res = oracle_of(oracle, inp.x, d, inp.z)
+    x = inp.x.cuda()
+    out = ga.gelu_and_mul_sparse(x, inp.z, d=d)
+    torch.cuda.synchronize()
+    check_gelu(out.cpu(), inp.x, d, res, f"strided d{d}+{extra}")
+
+
+@pytest.mark.parametrize("offset", [1, 2, 3, 4])
+def test_misaligned_input_pointer(ga, oracle, offset):
+    d, T = 2048, 6
+    inp = W.iid(T, d, seed=offset)
+    big = torch.zeros((T * 2 * d + 8,), dtype=torch.bfloat16)
+    big[offset:offset + T * 2 * d] = inp.x.reshape(-1)
+    gbig = big.cuda()
+    x = gbig[offset:offset + T * 2 * d].view(T, 2 * d)
+    out = ga.gelu_and_mul_sparse(x, inp.z)
+    torch.cuda.synchronize()
+    res = oracle_of(oracle, inp.x, d, inp.z)
+    check_gelu(out.cpu(), inp.x, d, res, f"offset {offset}")
+
+
+def test_guard_bands_untouched(ga, oracle):
+    for T, d in ((4, 2048), (64, 8192), (5, 31), (3, 32768), (2048, 4096)):
+        inp = W.iid(T, d, seed=T + d)
+        buf, out = guarded_empty((T, d))
+        ga.gelu_and_mul_sparse(inp.x.cuda(), inp.z, out=out)
+        torch.cuda.synchronize()
+        assert guards_intact(buf), (T, d)
+        check_gelu(out.cpu(), inp.x, d, oracle_of(oracle, inp.x, d, inp.z), f"guard T{T} d{d}")
+
+
+def test_nan_poisons_only_its_row(ga, oracle):
+    inp = W.iid(6, 2048, seed=17)
+    x = inp.x.clone()
+    x[2, 100] = float("nan")            # in the gate: row 2 all NaN
+    x[4, 2048 + 7] = float("nan")       # in up: one element
+    out = run(ga, x, 2048, inp.z)
+    res = oracle_of(oracle, x, 2048, inp.z)
+    check_gelu(out, x, 2048, res, "nan")
+    o = out.float()
+    assert torch.isnan(o[2]).all()
+    assert torch.isnan(o[4]).sum().item() <= 1
+    assert not torch.isnan(o[[0, 1, 3, 5]]).any()
+
+
+def test_zero_rows(ga):
+    x = torch.empty((0, 4096), dtype=torch.bfloat16, device="cuda")
+    out = ga.gelu_and_mul_sparse(x, W.Z95)
+    assert out.shape == (0, 2048)
+
+
+@pytest.mark.parametrize("T,d", [(3, 131072), (2, 262144), (2, 262152), (2, 1 << 20)])
+def test_widest_rows(ga, oracle, T, d):
+    inp = W.iid(T, d, seed=d)
+    res = oracle_of(oracle, inp.x, d, inp.z)
+    out = run(ga, inp.x, d, inp.z)
+    check_gelu(out, inp.x, d, res, f"wide d{d}")
+
+
+def test_many_short_rows(ga, oracle):
+    inp = W.iid(100003, 8, seed=5)
+    res = oracle_of(oracle, inp.x, 8, inp.z)
+    out = run(ga, inp.x, 8, inp.z)
+    check_gelu(out, inp.x, 8, res, "many rows")
+
+
+def test_side_stream_and_graph_capture(ga):
+    inps = [W.sweep(T, d, const_rows=False) for T, d in ((8, 8192), (256, 4096), (2048, 2048))]
+    xs = [i.x.cuda() for i in inps]
+    eager = [ga.gelu_and_mul_sparse(x, W.Z95) for x in xs]
+    outs = [torch.empty_like(e) for e in eager]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for x, o in zip(xs, outs):
+            ga.gelu_and_mul_sparse(x, W.Z95, out=o)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    for e, o in zip(eager, outs):
+        assert torch.equal(e.view(torch.int16), o.view(torch.int16))
+    for o in outs:
+        o.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for x, o in zip(xs, outs):
+            ga.gelu_and_mul_sparse(x, W.Z95, out=o)
+    g.replay()
+    torch.cuda.synchronize()
+    for e, o in zip(eager, outs):
+        assert torch.equal(e.view(torch.int16), o.view(torch.int16))
