@@ -22,12 +22,13 @@ OK = 0
 ERR_NULL, ERR_SIZE, ERR_STRIDE, ERR_TOO_LARGE = -1, -2, -3, -4
 ERR_OVERLAP, ERR_VARIANT, ERR_CUDA, ERR_ALIGN = -5, -6, -7, -8
 
-VARIANT_AUTO, VARIANT_WARP_ROWS, VARIANT_CTA_ROW, VARIANT_SCALAR = 0, 1, 2, 3
-VARIANT_NAMES = {0: "auto", 1: "warp_rows", 2: "cta_row", 3: "scalar"}
+VARIANT_AUTO, VARIANT_WARP_ROWS, VARIANT_CTA_ROW, VARIANT_SCALAR, VARIANT_TMA_ROWS = 0, 1, 2, 3, 4
+VARIANT_NAMES = {0: "auto", 1: "warp_rows", 2: "cta_row", 3: "scalar", 4: "tma_rows"}
 
 EXPORTED = (
     "gelu_and_mul_sparse", "silu_and_mul", "gated_act_status_string",
     "gated_act_last_cuda_error", "gelu_and_mul_sparse_plan", "gelu_and_mul_sparse_ex",
+    "gated_act_device_status",
 )
 
 
@@ -42,14 +43,16 @@ class Plan(ctypes.Structure):
 
     _fields_ = [("variant", ctypes.c_int32), ("cluster", ctypes.c_int32),
                 ("threads", ctypes.c_int32), ("vec_per_thread", ctypes.c_int32),
-                ("rows_per_cta", ctypes.c_int32), ("reserved", ctypes.c_int32),
-                ("grid", ctypes.c_int64)]
+                ("rows_per_cta", ctypes.c_int32), ("stages", ctypes.c_int32),
+                ("ctas_per_sm", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("grid", ctypes.c_int64), ("smem_bytes", ctypes.c_int64)]
 
     def as_dict(self) -> dict:
         return {"variant": VARIANT_NAMES.get(self.variant, str(self.variant)),
                 "cluster": self.cluster, "threads": self.threads,
                 "vec_per_thread": self.vec_per_thread, "rows_per_cta": self.rows_per_cta,
-                "grid": self.grid}
+                "stages": self.stages, "ctas_per_sm": self.ctas_per_sm, "grid": self.grid,
+                "smem_bytes": self.smem_bytes}
 
 
 _lib: ctypes.CDLL | None = None
@@ -81,6 +84,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.gated_act_status_string.restype = ctypes.c_char_p
     lib.gated_act_last_cuda_error.argtypes = []
     lib.gated_act_last_cuda_error.restype = ctypes.c_int
+    lib.gated_act_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint)]
+    lib.gated_act_device_status.restype = ctypes.c_int
     if path is None:
         _lib = lib
     return lib
@@ -155,6 +160,16 @@ def gelu_and_mul_sparse_plan(x: torch.Tensor, d: int | None = None, out: torch.T
     return p.as_dict()
 
 
+def device_status() -> int:
+    """Status bits the library's kernels raised on the current device (then cleared).
+
+    Bit 0: a bounded wait for a bulk copy gave up.  Synchronizes the device.
+    """
+    v = ctypes.c_uint(0)
+    _check("gated_act_device_status", load_library().gated_act_device_status(ctypes.byref(v)))
+    return int(v.value)
+
+
 def silu_and_mul(x: torch.Tensor, out: torch.Tensor | None = None,
                  stream: torch.cuda.Stream | None = None) -> torch.Tensor:
     """silu(gate) * up of a contiguous [M, 2d] bf16 CUDA tensor: returns [M, d] bf16."""
@@ -173,5 +188,6 @@ def silu_and_mul(x: torch.Tensor, out: torch.Tensor | None = None,
     return out
 
 
-__all__ = ["gelu_and_mul_sparse", "gelu_and_mul_sparse_plan", "silu_and_mul", "load_library",
+__all__ = ["gelu_and_mul_sparse", "gelu_and_mul_sparse_plan", "silu_and_mul", "device_status",
+           "load_library",
            "status_string", "GatedActError", "Plan", "EXPORTED", "LIB_PATH"]

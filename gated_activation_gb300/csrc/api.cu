@@ -1,5 +1,6 @@
 // Status strings, per-thread CUDA error record and cached device facts.
 #include <atomic>
+#include <cstdlib>
 
 #include "common.cuh"
 
@@ -28,6 +29,14 @@ int device_sm_count() {
     if (dev < kMaxDevices)
         g_sm_count[dev].store(n, std::memory_order_relaxed);
     return n;
+}
+
+bool pdl_enabled() {
+    static const bool on = [] {
+        const char *v = std::getenv("GATED_ACT_PDL");
+        return !(v && v[0] == '0' && v[1] == '\0');
+    }();
+    return on;
 }
 
 int cuda_status(cudaError_t e) {

@@ -44,6 +44,17 @@ __device__ __forceinline__ void st_vec(void *p, uint4 v) {
                  : "memory");
 }
 
+// Programmatic dependent launch.  Every kernel of the library waits for the
+// preceding grid in its stream to finish (and its memory to be visible)
+// before it touches global memory, and then lets the next PDL-launched grid
+// in the stream begin launching, so that grid's launch latency and set-up
+// overlap this one's tail.  Both are no-ops for a launch without the
+// programmatic-serialization attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Butterfly sum: every lane ends with the same bits (fp add is commutative
 // and each step pairs the same two operands in both partner lanes).
 __device__ __forceinline__ float warp_sum(float v) {
@@ -57,6 +68,39 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 // Per-device facts, queried once per device and cached.
 int device_sm_count();
+
+// Programmatic dependent launch is on unless the environment variable
+// GATED_ACT_PDL is "0" when the library makes its first launch.
+bool pdl_enabled();
+
+// Launch `kernel` on `stream` with programmatic stream serialization (when
+// enabled) and, for cluster > 1, a 1-D cluster of that many CTAs.
+template <typename... Exp, typename... Act>
+cudaError_t launch_kernel(void (*kernel)(Exp...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t stream, int cluster, Act &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    unsigned n = 0;
+    if (cluster > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = static_cast<unsigned>(cluster);
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    if (pdl_enabled()) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Act &&>(args)...);
+}
 
 // Record a CUDA error for gated_act_last_cuda_error() and map it to a status.
 int cuda_status(cudaError_t e);

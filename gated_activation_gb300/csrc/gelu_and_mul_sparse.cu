@@ -8,20 +8,33 @@
 //   out  = gelu_tanh(max(g - cutoff, 0)) * u,  fp32 math, one bf16 rounding.
 //
 // Every geometry reads each input element from HBM exactly once and keeps the
-// row on chip (registers) between the statistics and the epilogue:
+// row on chip between the statistics and the epilogue:
+//   * tma rows    -- persistent CTAs; each streams its rows' gate and up halves
+//                    through a ring of shared-memory slots with 1-D bulk copies
+//                    (cp.async.bulk, completion on mbarriers), so HBM keeps
+//                    streaming while earlier rows are reduced and written;
 //   * warp rows   -- one warp per row, shuffles only (d <= 2048);
 //   * CTA row     -- one CTA per row, or a cluster of C CTAs per row, each CTA
-//                    holding a column slice; CTA partials (count, sum, M2)
-//                    are exchanged through distributed shared memory and
-//                    merged with the pairwise update of Chan, Golub and LeVeque
-//                    (1979), so one cluster barrier serves mean and variance;
+//                    holding a column slice in registers; CTA partials (count,
+//                    sum, M2) are exchanged through distributed shared memory
+//                    and merged with the pairwise update of Chan, Golub and
+//                    LeVeque (1979), so one cluster barrier serves mean and
+//                    variance;
 //   * scalar      -- any alignment or width: 2-byte loads, gate re-read from
 //                    L1/L2 for each pass.
+// The fp32 arithmetic uses Blackwell's paired-lane instructions (add/sub/mul/
+// fma .f32x2), one instruction per two elements.
 #include <algorithm>
+#include <atomic>
 
 #include "common.cuh"
 
 namespace gact {
+
+// Device status word of this library (bit 0: a bounded wait for a bulk copy
+// gave up).  Read and cleared by gated_act_device_status().
+__device__ unsigned int g_device_status;
+
 namespace {
 
 constexpr float kSqrt2OverPi = 0.7978845608028654f;        // sqrt(2/pi)
@@ -30,9 +43,56 @@ constexpr float kCubicCoef = 0.7978845608028654f * 0.044715f;
 constexpr int kWarpRowsThreads = 128;      // 4 rows per CTA in the warp-rows geometry
 constexpr int kMaxCluster = 8;             // portable cluster size
 constexpr int kMaxSliceVec = 4096;         // 16-byte gate vectors one CTA can hold (1024 x 4)
-constexpr int kSplitSliceVec = 2048;       // split rows wider than this across a cluster
-constexpr int kMinSliceVec = 256;          // do not split rows below this per CTA
+constexpr int kMinSliceVec = 256;          // slices up to this use 2 vectors per thread
+constexpr int kFewRows = 8;                // up to this many rows of d >= 16384 use clusters
 constexpr int kScalarThreads = 256;
+
+constexpr int kTmaMaxStages = 8;
+constexpr int kTmaSmemPerSm = 228 * 1024;  // shared memory of one SM (1 KB per CTA is reserved)
+constexpr int kTmaSmemPerCta = 227 * 1024; // largest opt-in shared memory of one CTA
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;   // 1 s bound on every mbarrier wait
+
+// ------------------------------------------------------------ paired fp32 math
+__device__ __forceinline__ unsigned long long u64_of(float2 v) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(v.x), "f"(v.y));
+    return r;
+}
+__device__ __forceinline__ float2 f2_of(unsigned long long r) {
+    float2 v;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
+    return v;
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+    unsigned long long d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(u64_of(a)), "l"(u64_of(b)));
+    return f2_of(d);
+}
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+    unsigned long long d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(u64_of(a)), "l"(u64_of(b)));
+    return f2_of(d);
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+    unsigned long long d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(u64_of(a)), "l"(u64_of(b)));
+    return f2_of(d);
+}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(u64_of(a)), "l"(u64_of(b)), "l"(u64_of(c)));
+    return f2_of(d);
+}
+// max(x, 0) that returns NaN for a NaN input (fmaxf would return 0).
+__device__ __forceinline__ float relu_nan(float x) {
+    float y;
+    asm("max.NaN.f32 %0, %1, 0f00000000;" : "=f"(y) : "f"(x));
+    return y;
+}
+// bf16x2 word -> (low element, high element) as fp32
+__device__ __forceinline__ float2 unpack2(uint32_t w) {
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
 
 // tanh via the hardware approximation (PTX ISA tanh.approx.f32, maximum
 // relative error about 2^-11).  In gelu_tanh the argument is never negative,
@@ -43,43 +103,41 @@ __device__ __forceinline__ float tanh_approx(float x) {
     return y;
 }
 
-// gelu_tanh(max(g - cutoff, 0)) * u.  The comparison form of relu keeps a NaN
-// (fmaxf would turn it into 0).
-__device__ __forceinline__ float sparse_gelu_mul(float g, float u, float cutoff) {
-    float s = g - cutoff;
-    s = (s < 0.f) ? 0.f : s;
-    const float y = s * fmaf(kCubicCoef, s * s, kSqrt2OverPi);
-    const float h = 0.5f * s;
-    return fmaf(h, tanh_approx(y), h) * u;
+// Two outputs gelu_tanh(max(g - cutoff, 0)) * u from one gate word and one up word.
+__device__ __forceinline__ uint32_t epi2(uint32_t gw, uint32_t uw, float2 c2) {
+    float2 s = sub2(unpack2(gw), c2);
+    s.x = relu_nan(s.x);
+    s.y = relu_nan(s.y);
+    const float2 y = mul2(s, fma2(mul2(s, s), make_float2(kCubicCoef, kCubicCoef),
+                                  make_float2(kSqrt2OverPi, kSqrt2OverPi)));
+    const float2 h = mul2(s, make_float2(0.5f, 0.5f));
+    const float2 a = fma2(h, make_float2(tanh_approx(y.x), tanh_approx(y.y)), h);
+    const float2 o = mul2(a, unpack2(uw));
+    return pack_bf16x2(o.x, o.y);
 }
 
-__device__ __forceinline__ uint32_t epi2(uint32_t g, uint32_t u, float c) {
-    return pack_bf16x2(sparse_gelu_mul(bf16_lo(g), bf16_lo(u), c),
-                       sparse_gelu_mul(bf16_hi(g), bf16_hi(u), c));
+__device__ __forceinline__ uint4 epilogue8(uint4 g, uint4 u, float cutoff) {
+    const float2 c2 = make_float2(cutoff, cutoff);
+    return make_uint4(epi2(g.x, u.x, c2), epi2(g.y, u.y, c2), epi2(g.z, u.z, c2),
+                      epi2(g.w, u.w, c2));
 }
 
-__device__ __forceinline__ uint4 epilogue8(uint4 g, uint4 u, float c) {
-    return make_uint4(epi2(g.x, u.x, c), epi2(g.y, u.y, c), epi2(g.z, u.z, c),
-                      epi2(g.w, u.w, c));
+// Running pair sums over 8 gate values.
+__device__ __forceinline__ float2 sum8(float2 acc, uint4 g) {
+    acc = add2(acc, unpack2(g.x));
+    acc = add2(acc, unpack2(g.y));
+    acc = add2(acc, unpack2(g.z));
+    return add2(acc, unpack2(g.w));
 }
-
-__device__ __forceinline__ float sum8(uint4 g) {
-    return ((bf16_lo(g.x) + bf16_hi(g.x)) + (bf16_lo(g.y) + bf16_hi(g.y))) +
-           ((bf16_lo(g.z) + bf16_hi(g.z)) + (bf16_lo(g.w) + bf16_hi(g.w)));
-}
-
-__device__ __forceinline__ float sq(float x) { return x * x; }
-
-// sum over the 8 values of (x - m)^2
-__device__ __forceinline__ float ssd8(uint4 g, float m) {
-    float a = sq(bf16_lo(g.x) - m), b = sq(bf16_hi(g.x) - m);
-    a = fmaf(bf16_lo(g.y) - m, bf16_lo(g.y) - m, a);
-    b = fmaf(bf16_hi(g.y) - m, bf16_hi(g.y) - m, b);
-    a = fmaf(bf16_lo(g.z) - m, bf16_lo(g.z) - m, a);
-    b = fmaf(bf16_hi(g.z) - m, bf16_hi(g.z) - m, b);
-    a = fmaf(bf16_lo(g.w) - m, bf16_lo(g.w) - m, a);
-    b = fmaf(bf16_hi(g.w) - m, bf16_hi(g.w) - m, b);
-    return a + b;
+__device__ __forceinline__ float2 ssd8(float2 acc, uint4 g, float2 m2) {
+    float2 e = sub2(unpack2(g.x), m2);
+    acc = fma2(e, e, acc);
+    e = sub2(unpack2(g.y), m2);
+    acc = fma2(e, e, acc);
+    e = sub2(unpack2(g.z), m2);
+    acc = fma2(e, e, acc);
+    e = sub2(unpack2(g.w), m2);
+    return fma2(e, e, acc);
 }
 
 // CTA-wide sum; every thread returns the same bits.
@@ -116,6 +174,164 @@ __device__ __forceinline__ float ld_peer(const float *local, uint32_t rank) {
     return v;
 }
 
+// ------------------------------------------------------------ mbarrier + bulk copy
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+// 1-D bulk copy global -> this CTA's shared memory, completing on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
+                                          uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+// Wait for the phase `parity` of `bar`, giving up after kWaitLimitNs.
+__device__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const unsigned long long t0 = globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if ((i & 255u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs)
+            return false;
+    }
+}
+
+// ------------------------------------------------------------ tma rows
+// Persistent CTA b handles rows b, b + G, b + 2G, ... (G = gridDim.x).  Its
+// k-th row contributes chunk 2k (gate, 2d bytes) and chunk 2k+1 (up); chunk c
+// lands in slot c mod S, guarded by mbarrier c mod S at phase parity (c / S)
+// mod 2.  Thread 0 refills a slot once every thread is past the barrier that
+// follows the slot's last read: at the first CTA barrier of row k, chunks up
+// to 2k are consumed (gate k is in registers, up k-1 was consumed by row
+// k-1's epilogue), so chunks up to 2k + S may be in flight.
+template <int NT, int V>
+__global__ void __launch_bounds__(NT, (1024 / NT) > 0 ? (1024 / NT) : 1)
+gelu_tma_rows(uint16_t *__restrict__ out, const uint16_t *__restrict__ in, int64_t T, int d,
+              int64_t rs, float z, int S) {
+    constexpr int NW = NT / 32;
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ float red[2][NW];
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t chunk = 2u * static_cast<uint32_t>(d);
+    const uint32_t base = smem_addr(smem);
+    const uint32_t bars = base + static_cast<uint32_t>(S) * chunk;
+    const int64_t G = gridDim.x;
+    const int64_t nrows = blockIdx.x < T ? (T - 1 - blockIdx.x) / G + 1 : 0;
+    const int64_t nchunks = 2 * nrows;
+    const int nvec = d >> 3;
+
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s)
+            mbar_init(bars + 8u * s, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    pdl_wait();
+    pdl_trigger();
+
+    int64_t issued = 0;   // thread 0: next chunk to issue
+    auto issue_upto = [&](int64_t last) {
+        if (tid != 0)
+            return;
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        for (; issued < nchunks && issued <= last; ++issued) {
+            const int64_t row = blockIdx.x + (issued >> 1) * G;
+            const uint16_t *src = in + row * rs + ((issued & 1) ? d : 0);
+            const uint32_t slot = static_cast<uint32_t>(issued % S);
+            mbar_expect_tx(bars + 8u * slot, chunk);
+            bulk_load(base + slot * chunk, src, chunk, bars + 8u * slot);
+        }
+    };
+    issue_upto(S - 1);
+
+    bool bad = false;
+    int64_t k = 0;
+    for (; k < nrows; ++k) {
+        const int64_t row = blockIdx.x + k * G;
+        const int64_t cg = 2 * k, cu = 2 * k + 1;
+        const uint32_t sg = static_cast<uint32_t>(cg % S), su = static_cast<uint32_t>(cu % S);
+        bad |= !mbar_wait(bars + 8u * sg, static_cast<uint32_t>((cg / S) & 1));
+
+        const uint4 *gs = reinterpret_cast<const uint4 *>(smem + static_cast<size_t>(sg) * chunk);
+        uint4 g[V];
+#pragma unroll
+        for (int i = 0; i < V; ++i) {
+            const int v = tid + NT * i;
+            g[i] = v < nvec ? gs[v] : make_uint4(0u, 0u, 0u, 0u);
+        }
+        float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < V; ++i)
+            acc = sum8(acc, g[i]);
+        float s = warp_sum(acc.x + acc.y);
+        if (lane == 0)
+            red[0][warp] = s;
+        if (__syncthreads_or(bad))
+            break;
+        s = warp_sum(lane < NW ? red[0][lane] : 0.f);
+        issue_upto(cg + S);
+
+        const float mean = __fdiv_rn(s, static_cast<float>(d));
+        const float2 m2 = make_float2(mean, mean);
+        acc = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < V; ++i)
+            if (tid + NT * i < nvec)
+                acc = ssd8(acc, g[i], m2);
+        const float q = block_sum<NW>(acc.x + acc.y, red[1], lane, warp);
+        const float sd = __fsqrt_rn(__fdiv_rn(q, static_cast<float>(d)));
+        const float cutoff = fmaf(sd, z, mean);
+
+        bad |= !mbar_wait(bars + 8u * su, static_cast<uint32_t>((cu / S) & 1));
+        if (!bad) {
+            const uint4 *us = reinterpret_cast<const uint4 *>(smem + static_cast<size_t>(su) * chunk);
+            uint16_t *op = out + row * static_cast<int64_t>(d);
+#pragma unroll
+            for (int i = 0; i < V; ++i) {
+                const int v = tid + NT * i;
+                if (v < nvec)
+                    st_vec(op + 8 * v, epilogue8(g[i], us[v], cutoff));
+            }
+        }
+    }
+    // Every thread reaches this vote (the break above is CTA-uniform).  If a
+    // wait gave up, record it and let thread 0 wait, bounded again, for every
+    // copy it issued that was not consumed (from the up half of the row before
+    // the one in progress), so none is in flight when the CTA exits.
+    if (__syncthreads_or(bad) && tid == 0) {
+        atomicOr(&g_device_status, 1u);
+        for (int64_t c = k > 0 ? 2 * k - 1 : 0; c < issued; ++c)
+            mbar_wait(bars + 8u * static_cast<uint32_t>(c % S),
+                      static_cast<uint32_t>((c / S) & 1));
+    }
+}
+
 // ------------------------------------------------------------ warp rows
 // One warp per row; lane l holds gate/up vectors l, l+32, ..., l+32(V-1).
 template <int V>
@@ -127,6 +343,8 @@ gelu_warp_rows(uint16_t *__restrict__ out, const uint16_t *__restrict__ in, int6
                         (threadIdx.x >> 5);
     if (row >= T)
         return;
+    pdl_wait();
+    pdl_trigger();
     const int nvec = d >> 3;
     const uint16_t *gp = in + row * rs;
     const uint16_t *up = gp + d;
@@ -143,18 +361,18 @@ gelu_warp_rows(uint16_t *__restrict__ out, const uint16_t *__restrict__ in, int6
             u[i] = g[i];
         }
     }
-    float s = 0.f;
+    float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
     for (int i = 0; i < V; ++i)
-        s += sum8(g[i]);
-    s = warp_sum(s);
-    const float mean = __fdiv_rn(s, static_cast<float>(d));
-    float q = 0.f;
+        acc = sum8(acc, g[i]);
+    const float mean = __fdiv_rn(warp_sum(acc.x + acc.y), static_cast<float>(d));
+    const float2 m2 = make_float2(mean, mean);
+    acc = make_float2(0.f, 0.f);
 #pragma unroll
     for (int i = 0; i < V; ++i)
         if (lane + 32 * i < nvec)
-            q += ssd8(g[i], mean);
-    q = warp_sum(q);
+            acc = ssd8(acc, g[i], m2);
+    const float q = warp_sum(acc.x + acc.y);
     const float sd = __fsqrt_rn(__fdiv_rn(q, static_cast<float>(d)));
     const float cutoff = fmaf(sd, z, mean);
 
@@ -189,6 +407,8 @@ gelu_cta_rows(uint16_t *__restrict__ out, const uint16_t *__restrict__ in, int64
     const int v1 = min(nvec, v0 + sv);
     const int nk = max(v1 - v0, 0) * 8;
     const int64_t nclusters = gridDim.x / C;
+    pdl_wait();
+    pdl_trigger();
 
     for (int64_t row = blockIdx.x / C; row < T; row += nclusters) {
         const uint16_t *gp = in + row * rs;
@@ -205,31 +425,33 @@ gelu_cta_rows(uint16_t *__restrict__ out, const uint16_t *__restrict__ in, int64
                 u[i] = g[i];
             }
         }
-        float s = 0.f;
+        float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
         for (int i = 0; i < V; ++i)
-            s += sum8(g[i]);
-        s = block_sum<NW>(s, red[0], lane, warp);
+            acc = sum8(acc, g[i]);
+        const float s = block_sum<NW>(acc.x + acc.y, red[0], lane, warp);
 
         float mean, var;
         if (!CL) {
             mean = __fdiv_rn(s, static_cast<float>(d));
-            float q = 0.f;
+            const float2 m2 = make_float2(mean, mean);
+            acc = make_float2(0.f, 0.f);
 #pragma unroll
             for (int i = 0; i < V; ++i)
                 if (v0 + tid + NT * i < v1)
-                    q += ssd8(g[i], mean);
-            q = block_sum<NW>(q, red[1], lane, warp);
-            var = __fdiv_rn(q, static_cast<float>(d));
+                    acc = ssd8(acc, g[i], m2);
+            var = __fdiv_rn(block_sum<NW>(acc.x + acc.y, red[1], lane, warp),
+                            static_cast<float>(d));
         } else {
             // local two-pass statistics of this CTA's slice ...
             const float mk = nk > 0 ? __fdiv_rn(s, static_cast<float>(nk)) : 0.f;
-            float q = 0.f;
+            const float2 m2 = make_float2(mk, mk);
+            acc = make_float2(0.f, 0.f);
 #pragma unroll
             for (int i = 0; i < V; ++i)
                 if (v0 + tid + NT * i < v1)
-                    q += ssd8(g[i], mk);
-            q = block_sum<NW>(q, red[1], lane, warp);
+                    acc = ssd8(acc, g[i], m2);
+            const float q = block_sum<NW>(acc.x + acc.y, red[1], lane, warp);
             if (tid == 0) {
                 xch[0] = static_cast<float>(nk);
                 xch[1] = s;
@@ -276,12 +498,21 @@ __device__ __forceinline__ float ld_bf16(const uint16_t *p) {
     return __uint_as_float(static_cast<uint32_t>(ld_stream_u16(p)) << 16);
 }
 
+__device__ __forceinline__ float sparse_gelu_mul(float g, float u, float cutoff) {
+    const float s = relu_nan(g - cutoff);
+    const float y = s * fmaf(kCubicCoef, s * s, kSqrt2OverPi);
+    const float h = 0.5f * s;
+    return fmaf(h, tanh_approx(y), h) * u;
+}
+
 __global__ void __launch_bounds__(kScalarThreads)
 gelu_scalar_rows(uint16_t *__restrict__ out, const uint16_t *__restrict__ in, int64_t T,
                  int64_t d, int64_t rs, float z) {
     constexpr int NW = kScalarThreads / 32;
     __shared__ float red[2][NW];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    pdl_wait();
+    pdl_trigger();
     for (int64_t row = blockIdx.x; row < T; row += gridDim.x) {
         const uint16_t *gp = in + row * rs;
         const uint16_t *up = gp + d;
@@ -309,6 +540,7 @@ gelu_scalar_rows(uint16_t *__restrict__ out, const uint16_t *__restrict__ in, in
 // ------------------------------------------------------------ host side
 using WarpFn = void (*)(uint16_t *, const uint16_t *, int64_t, int, int64_t, float);
 using CtaFn = void (*)(uint16_t *, const uint16_t *, int64_t, int, int64_t, float, int, int);
+using TmaFn = void (*)(uint16_t *, const uint16_t *, int64_t, int, int64_t, float, int);
 
 WarpFn warp_fn(int v) {
     switch (v) {
@@ -346,6 +578,18 @@ CtaFn cta_fn(int nt, int v, int cluster) {
     return cluster > 1 ? cta_fn_t<true>(nt, v) : cta_fn_t<false>(nt, v);
 }
 
+TmaFn tma_fn(int nt) {
+    switch (nt) {
+    case 32: return gelu_tma_rows<32, 4>;
+    case 64: return gelu_tma_rows<64, 4>;
+    case 128: return gelu_tma_rows<128, 4>;
+    case 256: return gelu_tma_rows<256, 4>;
+    case 512: return gelu_tma_rows<512, 4>;
+    case 1024: return gelu_tma_rows<1024, 4>;
+    default: return nullptr;
+    }
+}
+
 int pow2_ceil(int64_t x) {
     int p = 1;
     while (p < x)
@@ -369,6 +613,48 @@ void cta_shape(int64_t sv, int *nt, int *v) {
         *v = 4;
         *nt = std::max(64, pow2_ceil(ceil_div(sv, 4)));
     }
+}
+
+// TMA rows geometry for a row of nvec gate vectors.  An SM runs 1024
+// threads (64 registers each) split into cps CTAs of NT = 1024 / cps threads
+// (fewer when the row is short), so cps rows are in progress per SM and one
+// row's reduce/barrier latency overlaps the others' arithmetic.  Each CTA
+// gets 1/cps of the SM's shared memory and at least three slots (the next
+// row's gate and up stream in while a row is finished; two when a single CTA
+// holds the widest rows).  want_cps = 0 picks cps; otherwise it is forced.
+// Returns false when the row does not fit.
+bool tma_shape_for(int64_t nvec, int c, int *nt, int *stages, int64_t *smem) {
+    const int64_t chunk = 16 * nvec;                        // bytes of a gate (or up) half-row
+    const int n = std::min(1024 / c, std::max(32, pow2_ceil(nvec)));
+    if (n < 32 || ceil_div(nvec, n) > 4)
+        return false;
+    const int64_t per_cta = std::min<int64_t>(kTmaSmemPerSm / c, kTmaSmemPerCta) - 1536;
+    const int64_t s = std::min<int64_t>(kTmaMaxStages, (per_cta - 8 * kTmaMaxStages) / chunk);
+    if (s < 3 && !(c == 1 && s >= 2))
+        return false;
+    *nt = n;
+    *stages = static_cast<int>(s);
+    *smem = s * chunk + 8 * s;
+    return true;
+}
+
+bool tma_shape(int64_t nvec, int want_cps, int *cps, int *nt, int *stages, int64_t *smem) {
+    if (want_cps > 0) {
+        if (want_cps > 16 || (want_cps & (want_cps - 1)) != 0)
+            return false;
+        *cps = want_cps;
+        return tma_shape_for(nvec, want_cps, nt, stages, smem);
+    }
+    // default: four 16-byte gate vectors per thread (the most cps that fits)
+    for (int c = 16; c >= 1; c /= 2) {
+        if (1024 / c < ceil_div(nvec, 4))
+            continue;
+        if (tma_shape_for(nvec, c, nt, stages, smem)) {
+            *cps = c;
+            return true;
+        }
+    }
+    return false;
 }
 
 // check_ptrs = false (plan queries): pointers are only inspected for alignment.
@@ -398,7 +684,7 @@ int make_plan(const void *out, const void *in, int64_t T, int64_t d, int64_t rs,
     const int rc = validate(out, in, T, d, rs, check_ptrs);
     if (rc != GATED_ACT_OK)
         return rc;
-    if (variant < GATED_ACT_VARIANT_AUTO || variant > GATED_ACT_VARIANT_SCALAR)
+    if (variant < GATED_ACT_VARIANT_AUTO || variant > GATED_ACT_VARIANT_TMA_ROWS)
         return GATED_ACT_ERR_VARIANT;
     gated_act_plan &q = p->pub;
     q = gated_act_plan{};
@@ -406,16 +692,41 @@ int make_plan(const void *out, const void *in, int64_t T, int64_t d, int64_t rs,
     const bool vec_ok = aligned(in, 16) && aligned(out, 16) && d % 8 == 0 && rs % 8 == 0;
     const int64_t nvec = d / 8;
     const int sms = sm_count > 0 ? sm_count : (T > 0 ? device_sm_count() : 1);
+    int t_cps = 0, t_nt = 0, t_stages = 0;
+    int64_t t_smem = 0;
+    const int want_cps = variant == GATED_ACT_VARIANT_TMA_ROWS ? cluster : 0;
+    const bool tma_ok = vec_ok && tma_shape(nvec, want_cps, &t_cps, &t_nt, &t_stages, &t_smem);
 
+    // Measured on GB300 (every geometry timed per T x d, graph-replayed over
+    // rotating buffers): persistent TMA rows win only for the widest rows at
+    // many rows per SM; one CTA per row wins everywhere else, except a handful
+    // of rows of d >= 16384, where 8-CTA clusters put more SMs on each row.
     if (variant == GATED_ACT_VARIANT_AUTO) {
+        const int64_t sm = static_cast<int64_t>(sms);
         if (!vec_ok || nvec > int64_t(kMaxSliceVec) * kMaxCluster)
             variant = GATED_ACT_VARIANT_SCALAR;
-        else if (nvec <= 256)
+        else if (tma_ok && ((nvec >= 4096 && T >= 3 * sm) || (nvec >= 2048 && T >= 12 * sm)))
+            variant = GATED_ACT_VARIANT_TMA_ROWS;
+        else if (nvec <= 64)
             variant = GATED_ACT_VARIANT_WARP_ROWS;
         else
             variant = GATED_ACT_VARIANT_CTA_ROW;
-        if (variant == GATED_ACT_VARIANT_CTA_ROW)
-            cluster = 0;
+        cluster = 0;
+    }
+
+    if (variant == GATED_ACT_VARIANT_TMA_ROWS) {
+        if (!tma_ok)
+            return GATED_ACT_ERR_VARIANT;
+        q.variant = variant;
+        q.cluster = 1;
+        q.threads = t_nt;
+        q.vec_per_thread = static_cast<int32_t>(ceil_div(nvec, t_nt));
+        q.rows_per_cta = 1;
+        q.ctas_per_sm = t_cps;
+        q.stages = t_stages;
+        q.smem_bytes = t_smem;
+        q.grid = std::min<int64_t>(T, static_cast<int64_t>(sms) * t_cps);
+        return GATED_ACT_OK;
     }
 
     if (variant == GATED_ACT_VARIANT_WARP_ROWS) {
@@ -438,10 +749,10 @@ int make_plan(const void *out, const void *in, int64_t T, int64_t d, int64_t rs,
         int C = cluster;
         if (C == 0) {
             C = 1;
-            while (ceil_div(nvec, C) > kSplitSliceVec && C < kMaxCluster)
+            while (ceil_div(nvec, C) > kMaxSliceVec && C < kMaxCluster)
                 C *= 2;
-            while (T * C < sms && C < kMaxCluster && ceil_div(nvec, 2 * C) >= kMinSliceVec)
-                C *= 2;
+            if (T <= kFewRows && nvec >= 2048)
+                C = kMaxCluster;
         }
         if (C < 1 || C > kMaxCluster || (C & (C - 1)) != 0)
             return GATED_ACT_ERR_VARIANT;
@@ -471,47 +782,70 @@ int make_plan(const void *out, const void *in, int64_t T, int64_t d, int64_t rs,
     return GATED_ACT_OK;
 }
 
+// Shared memory above 48 KB needs a per-kernel opt-in, done once per device;
+// the carveout hint asks for the largest shared-memory split of L1.
+int ensure_smem_attr(TmaFn fn, int nt) {
+    constexpr int kMaxDevices = 64;
+    static std::atomic<unsigned> done[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        dev = -1;
+    const unsigned bit = 1u << (31 - __builtin_clz(static_cast<unsigned>(nt)));
+    if (dev >= 0 && dev < kMaxDevices && (done[dev].load(std::memory_order_acquire) & bit))
+        return GATED_ACT_OK;
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, fn);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kTmaSmemPerCta - static_cast<int>(fa.sharedSizeBytes));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess)
+        return cuda_status(e);
+    if (dev >= 0 && dev < kMaxDevices)
+        done[dev].fetch_or(bit, std::memory_order_acq_rel);
+    return GATED_ACT_OK;
+}
+
 int launch(const Plan &p, void *out, const void *in, int64_t T, int64_t d, int64_t rs,
            double z, cudaStream_t stream) {
     uint16_t *o = static_cast<uint16_t *>(out);
     const uint16_t *x = static_cast<const uint16_t *>(in);
     const float zf = static_cast<float>(z);
+    const int di = static_cast<int>(d);
     const gated_act_plan &q = p.pub;
     const dim3 grid(static_cast<unsigned>(q.grid)), block(q.threads);
+    cudaError_t e = cudaSuccess;
     switch (q.variant) {
+    case GATED_ACT_VARIANT_TMA_ROWS: {
+        TmaFn fn = tma_fn(q.threads);
+        if (!fn)
+            return GATED_ACT_ERR_VARIANT;
+        const int rc = ensure_smem_attr(fn, q.threads);
+        if (rc != GATED_ACT_OK)
+            return rc;
+        e = launch_kernel(fn, grid, block, static_cast<size_t>(q.smem_bytes), stream, 1, o, x, T,
+                          di, rs, zf, static_cast<int>(q.stages));
+        break;
+    }
     case GATED_ACT_VARIANT_WARP_ROWS:
-        warp_fn(q.vec_per_thread)<<<grid, block, 0, stream>>>(o, x, T, static_cast<int>(d), rs, zf);
+        e = launch_kernel(warp_fn(q.vec_per_thread), grid, block, 0, stream, 1, o, x, T, di, rs, zf);
         break;
     case GATED_ACT_VARIANT_CTA_ROW: {
         CtaFn fn = cta_fn(q.threads, q.vec_per_thread, q.cluster);
         if (!fn)
             return GATED_ACT_ERR_VARIANT;
-        if (q.cluster == 1) {
-            fn<<<grid, block, 0, stream>>>(o, x, T, static_cast<int>(d), rs, zf, 1, p.sv);
-        } else {
-            cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = grid;
-            cfg.blockDim = block;
-            cfg.dynamicSmemBytes = 0;
-            cfg.stream = stream;
-            cudaLaunchAttribute attr[1];
-            attr[0].id = cudaLaunchAttributeClusterDimension;
-            attr[0].val.clusterDim.x = q.cluster;
-            attr[0].val.clusterDim.y = 1;
-            attr[0].val.clusterDim.z = 1;
-            cfg.attrs = attr;
-            cfg.numAttrs = 1;
-            const cudaError_t e = cudaLaunchKernelEx(&cfg, fn, o, x, T, static_cast<int>(d), rs,
-                                                     zf, static_cast<int>(q.cluster), p.sv);
-            if (e != cudaSuccess)
-                return cuda_status(e);
-        }
+        e = launch_kernel(fn, grid, block, 0, stream, q.cluster, o, x, T, di, rs, zf,
+                          static_cast<int>(q.cluster), p.sv);
         break;
     }
     default:
-        gelu_scalar_rows<<<grid, block, 0, stream>>>(o, x, T, d, rs, zf);
+        e = launch_kernel(gelu_scalar_rows, grid, block, 0, stream, 1, o, x, T, d, rs, zf);
         break;
     }
+    if (e != cudaSuccess)
+        return cuda_status(e);
     return cuda_status(cudaGetLastError());
 }
 
@@ -545,4 +879,19 @@ extern "C" int gelu_and_mul_sparse(void *out, const void *in, int64_t T, int64_t
                                    int64_t row_stride, double z, cudaStream_t stream) {
     return gelu_and_mul_sparse_ex(out, in, T, d, row_stride, z, GATED_ACT_VARIANT_AUTO, 0,
                                   stream);
+}
+
+extern "C" int gated_act_device_status(unsigned int *flags) {
+    if (!flags)
+        return GATED_ACT_ERR_NULL;
+    unsigned int v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, gact::g_device_status, sizeof v);
+    if (e != cudaSuccess)
+        return gact::cuda_status(e);
+    const unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(gact::g_device_status, &zero, sizeof zero);
+    if (e != cudaSuccess)
+        return gact::cuda_status(e);
+    *flags = v;
+    return GATED_ACT_OK;
 }

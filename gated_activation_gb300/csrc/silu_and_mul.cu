@@ -49,6 +49,8 @@ silu_vec(uint16_t *__restrict__ out, const uint16_t *__restrict__ in, Idx total,
          int64_t d) {
     const Idx nthreads = static_cast<Idx>(gridDim.x) * kSiluThreads;
     const Idx first = static_cast<Idx>(blockIdx.x) * kSiluThreads + threadIdx.x;
+    pdl_wait();
+    pdl_trigger();
     for (Idx base = first; base < total; base += nthreads * kVecPerThread) {
         uint4 g[kVecPerThread], u[kVecPerThread];
         Idx idx[kVecPerThread];
@@ -79,6 +81,8 @@ __global__ void __launch_bounds__(kSiluThreads)
 silu_scalar(uint16_t *__restrict__ out, const uint16_t *__restrict__ in, int64_t M, int64_t d) {
     const int64_t total = M * d;
     const int64_t step = static_cast<int64_t>(gridDim.x) * kSiluThreads;
+    pdl_wait();
+    pdl_trigger();
     for (int64_t e = static_cast<int64_t>(blockIdx.x) * kSiluThreads + threadIdx.x; e < total;
          e += step) {
         const int64_t r = e / d, c = e - r * d;
@@ -118,15 +122,21 @@ extern "C" int silu_and_mul(void *out, const void *in, int64_t M, int64_t d,
         const int64_t nv = d / 8, total = M * nv;
         const int64_t grid = std::min<int64_t>(
             ceil_div(ceil_div(total, kVecPerThread), kSiluThreads), 0x7FFFFFFF);
-        if (total < (int64_t(1) << 32) - int64_t(grid) * kSiluThreads * kVecPerThread)
-            silu_vec<uint32_t><<<static_cast<unsigned>(grid), kSiluThreads, 0, stream>>>(
-                o, x, static_cast<uint32_t>(total), static_cast<uint32_t>(nv), d);
-        else
-            silu_vec<uint64_t><<<static_cast<unsigned>(grid), kSiluThreads, 0, stream>>>(
-                o, x, static_cast<uint64_t>(total), static_cast<uint64_t>(nv), d);
+        const dim3 g(static_cast<unsigned>(grid)), b(kSiluThreads);
+        const cudaError_t e =
+            total < (int64_t(1) << 32) - int64_t(grid) * kSiluThreads * kVecPerThread
+                ? launch_kernel(silu_vec<uint32_t>, g, b, 0, stream, 1, o, x,
+                                static_cast<uint32_t>(total), static_cast<uint32_t>(nv), d)
+                : launch_kernel(silu_vec<uint64_t>, g, b, 0, stream, 1, o, x,
+                                static_cast<uint64_t>(total), static_cast<uint64_t>(nv), d);
+        if (e != cudaSuccess)
+            return cuda_status(e);
     } else {
         const int64_t grid = std::min<int64_t>(ceil_div(M * d, kSiluThreads), int64_t(1) << 20);
-        silu_scalar<<<static_cast<unsigned>(grid), kSiluThreads, 0, stream>>>(o, x, M, d);
+        const cudaError_t e = launch_kernel(silu_scalar, dim3(static_cast<unsigned>(grid)),
+                                            dim3(kSiluThreads), 0, stream, 1, o, x, M, d);
+        if (e != cudaSuccess)
+            return cuda_status(e);
     }
     return cuda_status(cudaGetLastError());
 }

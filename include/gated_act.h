@@ -96,6 +96,15 @@ const char *gated_act_status_string(int status);
 /* The cudaError_t behind the calling thread's last GATED_ACT_ERR_CUDA (0 if none). */
 int gated_act_last_cuda_error(void);
 
+/*
+ * Device-side status of the library's kernels on the current device since
+ * the last call, then cleared.  *flags bit 0: a kernel's bounded wait (1 s)
+ * for one of its own bulk copies gave up; the rows that CTA had not finished
+ * were left unwritten.  No other bit is used.  Synchronizes the device
+ * (it copies a status word), so call it outside stream capture.
+ */
+int gated_act_device_status(unsigned int *flags);
+
 /* ------------------------------------------------------------------------
  * Launch-geometry control, for tests and measurements.
  *
@@ -108,7 +117,9 @@ typedef enum gated_act_variant {
     GATED_ACT_VARIANT_WARP_ROWS = 1, /* one warp per row, several rows per CTA     */
     GATED_ACT_VARIANT_CTA_ROW = 2,   /* one CTA, or a cluster of CTAs, per row;
                                         row held in registers                       */
-    GATED_ACT_VARIANT_SCALAR = 3     /* any layout: one CTA per row, 2-byte loads   */
+    GATED_ACT_VARIANT_SCALAR = 3,    /* any layout: one CTA per row, 2-byte loads   */
+    GATED_ACT_VARIANT_TMA_ROWS = 4   /* persistent CTAs; gate/up half-rows stream
+                                        through shared memory by bulk copy          */
 } gated_act_variant;
 
 typedef struct gated_act_plan {
@@ -117,8 +128,12 @@ typedef struct gated_act_plan {
     int32_t threads;        /* threads per CTA                                 */
     int32_t vec_per_thread; /* 16-byte vectors of gate per thread (0: scalar)  */
     int32_t rows_per_cta;   /* rows one CTA handles at a time                  */
+    int32_t stages;         /* shared-memory slots per CTA (TMA rows), else 0 */
+    int32_t ctas_per_sm;    /* resident CTAs per SM the grid is sized for
+                               (TMA rows), else 0                              */
     int32_t reserved;
     int64_t grid;           /* CTAs launched                                   */
+    int64_t smem_bytes;     /* dynamic shared memory per CTA                   */
 } gated_act_plan;
 
 /*
@@ -136,8 +151,14 @@ int gelu_and_mul_sparse_plan(const void *out, const void *in, int64_t T,
 /*
  * gelu_and_mul_sparse with a forced geometry.
  *   variant  a gated_act_variant; AUTO behaves like gelu_and_mul_sparse.
+ *            TMA_ROWS needs the 16-byte layout and d <= 32768; the first
+ *            TMA_ROWS launch of a kernel shape on a device raises that
+ *            kernel's shared-memory limit (cudaFuncSetAttribute), so make one
+ *            call per device before capturing such launches in a graph.
  *   cluster  for GATED_ACT_VARIANT_CTA_ROW: CTAs per row, a power of two
- *            in [1, 8], or 0 to let the library choose; ignored otherwise.
+ *            in [1, 8]; for GATED_ACT_VARIANT_TMA_ROWS: CTAs per SM, a power
+ *            of two in [1, 16] (threads per CTA = 1024 / that); 0 lets the
+ *            library choose; ignored by the other variants.
  * Returns GATED_ACT_ERR_VARIANT when the layout cannot use that geometry
  * (vector variants need the 16-byte layout above; a row slice must fit the
  * CTA's registers).

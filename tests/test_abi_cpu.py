@@ -101,20 +101,27 @@ def plan(lib, T, d, rs=None, variant=0, cluster=0, sms=GB300_SMS, out=0x10000, i
 
 
 def test_plan_geometry_families(lib):
-    # small d: a warp per row
-    rc, p = plan(lib, 2048, 2048)
-    assert rc == 0 and p["variant"] == "warp_rows" and p["vec_per_thread"] == 8
-    # large T, d = 16384: one CTA per row, whole grid of rows
+    # short rows: a warp per row
+    rc, p = plan(lib, 2048, 512)
+    assert rc == 0 and p["variant"] == "warp_rows" and p["vec_per_thread"] == 2
+    # d = 2048 .. 8192 at any T: one CTA per row, one row per CTA
+    for T, d in ((2048, 2048), (2048, 8192), (64, 8192), (1, 4096)):
+        rc, p = plan(lib, T, d)
+        assert rc == 0 and p["variant"] == "cta_row" and p["cluster"] == 1 and p["grid"] == T
+    # the widest rows at many rows per SM: persistent TMA rows, one wave of CTAs
     rc, p = plan(lib, 2048, 16384)
-    assert rc == 0 and p["variant"] == "cta_row" and p["cluster"] == 1 and p["grid"] == 2048
-    # d = 32768 is split across a 2-CTA cluster even at large T
-    rc, p = plan(lib, 2048, 32768)
-    assert rc == 0 and p["cluster"] == 2 and p["grid"] == 4096
-    # small T: rows split across clusters so more SMs take part
+    assert rc == 0 and p["variant"] == "tma_rows" and p["grid"] <= 16 * GB300_SMS
+    assert p["stages"] >= 2 and p["smem_bytes"] <= 227 * 1024
+    rc, p = plan(lib, 512, 32768)
+    assert rc == 0 and p["variant"] == "tma_rows" and p["threads"] == 1024
+    rc, p = plan(lib, 1024, 16384)
+    assert rc == 0 and p["variant"] == "cta_row" and p["threads"] == 512
+    # a handful of wide rows: 8-CTA clusters per row
     rc, p = plan(lib, 1, 32768)
-    assert rc == 0 and p["cluster"] == 8
-    rc, p = plan(lib, 64, 8192)
-    assert rc == 0 and p["cluster"] * 64 >= GB300_SMS
+    assert rc == 0 and p["variant"] == "cta_row" and p["cluster"] == 8
+    # rows wider than one CTA's registers are split across a cluster
+    rc, p = plan(lib, 2048, 65536, variant=ga.VARIANT_CTA_ROW)
+    assert rc == 0 and p["cluster"] == 2 and p["grid"] == 4096
 
 
 def test_plan_covers_every_slice(lib):
@@ -126,6 +133,11 @@ def test_plan_covers_every_slice(lib):
             nvec = d // 8
             if p["variant"] == "warp_rows":
                 assert 32 * p["vec_per_thread"] >= nvec
+            elif p["variant"] == "tma_rows":
+                assert p["threads"] * p["vec_per_thread"] >= nvec and p["vec_per_thread"] <= 4
+                # every CTA of an SM fits: slots of 2d bytes plus their barriers
+                assert p["smem_bytes"] == p["stages"] * (2 * d + 8)
+                assert p["stages"] >= 2 and p["smem_bytes"] <= 227 * 1024 - 1024
             elif p["variant"] == "cta_row":
                 sv = -(-nvec // p["cluster"])
                 assert p["threads"] * p["vec_per_thread"] >= sv
@@ -140,6 +152,18 @@ def test_plan_falls_back_to_scalar(lib):
     assert plan(lib, 4, 64, rs=130)[1]["variant"] == "scalar"    # row stride not 16-byte
     assert plan(lib, 4, 64, inp=0x100002)[1]["variant"] == "scalar"   # misaligned pointer
     assert plan(lib, 4, 262144 + 8)[1]["variant"] == "scalar"    # wider than 8 CTAs hold
+
+
+def test_plan_tma_rows_limits(lib):
+    for d in (64, 1024, 2048, 8192, 16384, 32768):
+        rc, p = plan(lib, 4096, d, variant=ga.VARIANT_TMA_ROWS)
+        assert rc == 0 and p["variant"] == "tma_rows"
+        cps = -(-p["grid"] // GB300_SMS)
+        assert cps * p["threads"] <= 2048 and cps * (p["smem_bytes"] + 1024) <= 228 * 1024
+    assert plan(lib, 4096, 32776, variant=ga.VARIANT_TMA_ROWS)[0] == ga.ERR_VARIANT
+    assert plan(lib, 4096, 31, variant=ga.VARIANT_TMA_ROWS)[0] == ga.ERR_VARIANT
+    assert plan(lib, 4096, 64, rs=130, variant=ga.VARIANT_TMA_ROWS)[0] == ga.ERR_VARIANT
+    assert plan(lib, 5, 8192, variant=ga.VARIANT_TMA_ROWS)[1]["grid"] == 5
 
 
 def test_plan_forced_variants(lib):
@@ -157,6 +181,8 @@ def test_plan_depends_only_on_arguments(lib):
     a = plan(lib, 64, 8192)
     b = plan(lib, 64, 8192)
     assert a == b
-    # a different SM count may change the split, never the validity
-    rc, p = plan(lib, 64, 8192, sms=32)
-    assert rc == 0 and p["cluster"] == 1
+    # a different SM count may change the choice, never the validity
+    rc, p = plan(lib, 1024, 32768, sms=32)
+    assert rc == 0 and p["variant"] == "tma_rows" and p["grid"] == 32
+    rc, p = plan(lib, 1024, 32768, sms=512)
+    assert rc == 0 and p["variant"] == "cta_row"

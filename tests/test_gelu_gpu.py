@@ -32,7 +32,7 @@ def oracle_of(oracle, x_cpu, d, z):
     return oracle.gelu_and_mul_sparse(W.to_bits(x_cpu.contiguous()), d=d, z=z)
 
 
-GEOMETRIES = [(0, 0), (1, 0), (2, 1), (2, 2), (2, 4), (2, 8), (3, 0)]
+GEOMETRIES = [(0, 0), (1, 0), (2, 1), (2, 2), (2, 4), (2, 8), (3, 0), (4, 0)]
 
 
 @pytest.mark.parametrize("variant,cluster", GEOMETRIES)
@@ -91,6 +91,30 @@ def test_sweep_shapes_every_cluster(ga, oracle, T, d, cluster):
     check_gelu(out, inp.x, d, res, f"{inp.name} c{cluster}")
 
 
+@pytest.mark.parametrize("T,d", [(2048, 2048), (1024, 4096), (512, 8192), (300, 16384),
+                                 (257, 32768), (5, 16384), (1, 2048), (1000, 1024), (777, 2056),
+                                 (333, 8200)])
+def test_tma_rows_forced(ga, oracle, T, d):
+    inp = W.iid(T, d, seed=T * 7 + d)
+    res = oracle_of(oracle, inp.x, d, inp.z)
+    out = run(ga, inp.x, d, inp.z, variant=4)
+    check_gelu(out, inp.x, d, res, f"tma T{T} d{d}")
+    assert ga.device_status() == 0
+
+
+def test_tma_rows_strided_and_constant_rows(ga, oracle):
+    inp = W.sweep(1024, 8192, const_rows=True)
+    res = oracle_of(oracle, inp.x, 8192, inp.z)
+    out = run(ga, inp.x, 8192, inp.z, variant=4)
+    check_gelu(out, inp.x, 8192, res, "tma sweep rows")
+    assert torch.count_nonzero(out[-3:].float()).item() == 0
+    inp = W.iid(700, 4096, seed=3, row_stride=8192 + 64)
+    res = oracle_of(oracle, inp.x, 4096, inp.z)
+    out = run(ga, inp.x, 4096, inp.z, variant=4)
+    check_gelu(out, inp.x, 4096, res, "tma strided")
+    assert ga.device_status() == 0
+
+
 def test_same_geometry_is_bitwise_deterministic(ga):
     inp = W.sweep(64, 8192, const_rows=False)
     x = inp.x.cuda()
@@ -137,13 +161,14 @@ def test_misaligned_input_pointer(ga, oracle, offset):
 
 
 def test_guard_bands_untouched(ga, oracle):
-    for T, d in ((4, 2048), (64, 8192), (5, 31), (3, 32768), (2048, 4096)):
+    for T, d, v in ((4, 2048, 0), (64, 8192, 0), (5, 31, 0), (3, 32768, 0), (2048, 4096, 0),
+                    (2048, 4096, 4), (600, 32768, 4), (7, 2048, 4)):
         inp = W.iid(T, d, seed=T + d)
         buf, out = guarded_empty((T, d))
-        ga.gelu_and_mul_sparse(inp.x.cuda(), inp.z, out=out)
+        ga.gelu_and_mul_sparse(inp.x.cuda(), inp.z, out=out, variant=v)
         torch.cuda.synchronize()
-        assert guards_intact(buf), (T, d)
-        check_gelu(out.cpu(), inp.x, d, oracle_of(oracle, inp.x, d, inp.z), f"guard T{T} d{d}")
+        assert guards_intact(buf), (T, d, v)
+        check_gelu(out.cpu(), inp.x, d, oracle_of(oracle, inp.x, d, inp.z), f"guard T{T} d{d} v{v}")
 
 
 def test_nan_poisons_only_its_row(ga, oracle):
@@ -181,8 +206,13 @@ def test_many_short_rows(ga, oracle):
     check_gelu(out, inp.x, 8, res, "many rows")
 
 
+def test_device_status_clear_after_the_suite(ga):
+    assert ga.device_status() == 0
+
+
 def test_side_stream_and_graph_capture(ga):
-    inps = [W.sweep(T, d, const_rows=False) for T, d in ((8, 8192), (256, 4096), (2048, 2048))]
+    inps = [W.sweep(T, d, const_rows=False) for T, d in ((8, 8192), (256, 4096), (2048, 2048),
+                                                          (2048, 16384))]
     xs = [i.x.cuda() for i in inps]
     eager = [ga.gelu_and_mul_sparse(x, W.Z95) for x in xs]
     outs = [torch.empty_like(e) for e in eager]
