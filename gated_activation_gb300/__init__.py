@@ -28,7 +28,7 @@ VARIANT_NAMES = {0: "auto", 1: "warp_rows", 2: "cta_row", 3: "scalar", 4: "tma_r
 EXPORTED = (
     "gelu_and_mul_sparse", "silu_and_mul", "gated_act_status_string",
     "gated_act_last_cuda_error", "gelu_and_mul_sparse_plan", "gelu_and_mul_sparse_ex",
-    "gated_act_device_status",
+    "gated_act_device_status", "gated_act_noop",
 )
 
 
@@ -86,6 +86,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.gated_act_last_cuda_error.restype = ctypes.c_int
     lib.gated_act_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint)]
     lib.gated_act_device_status.restype = ctypes.c_int
+    lib.gated_act_noop.argtypes = [vp]
+    lib.gated_act_noop.restype = ctypes.c_int
     if path is None:
         _lib = lib
     return lib
@@ -170,6 +172,11 @@ def device_status() -> int:
     return int(v.value)
 
 
+def noop(stream: torch.cuda.Stream | None = None) -> None:
+    """Launch the library's empty kernel (launch-overhead probe)."""
+    _check("gated_act_noop", load_library().gated_act_noop(_stream_handle(stream)))
+
+
 def silu_and_mul(x: torch.Tensor, out: torch.Tensor | None = None,
                  stream: torch.cuda.Stream | None = None) -> torch.Tensor:
     """silu(gate) * up of a contiguous [M, 2d] bf16 CUDA tensor: returns [M, d] bf16."""
@@ -188,6 +195,6 @@ def silu_and_mul(x: torch.Tensor, out: torch.Tensor | None = None,
     return out
 
 
-__all__ = ["gelu_and_mul_sparse", "gelu_and_mul_sparse_plan", "silu_and_mul", "device_status",
+__all__ = ["gelu_and_mul_sparse", "gelu_and_mul_sparse_plan", "silu_and_mul", "device_status", "noop",
            "load_library",
            "status_string", "GatedActError", "Plan", "EXPORTED", "LIB_PATH"]

@@ -46,7 +46,20 @@ int cuda_status(cudaError_t e) {
     return GATED_ACT_ERR_CUDA;
 }
 
+// Empty kernel with the library's launch attributes (launch-overhead probe).
+__global__ void noop_kernel() {
+    pdl_wait();
+    pdl_trigger();
+}
+
 }  // namespace gact
+
+extern "C" int gated_act_noop(cudaStream_t stream) {
+    const cudaError_t e = gact::launch_kernel(gact::noop_kernel, dim3(1), dim3(32), 0, stream, 1);
+    if (e != cudaSuccess)
+        return gact::cuda_status(e);
+    return gact::cuda_status(cudaGetLastError());
+}
 
 extern "C" const char *gated_act_status_string(int status) {
     switch (status) {

@@ -2,12 +2,10 @@
 //
 // Megatron-LM PR "Size MoE activation kernel grid to the row count",
 // sections "What changed and why" and "Correctness": a pure elementwise op
-// whose cost is launch geometry.  Here the grid is sized to the work -- every
-// thread owns kVecPerThread 16-byte output vectors spread over the whole
-// [M, d] output (consecutive threads take consecutive vectors, so every warp
-// access is one contiguous 512-byte run) -- and all loads are issued before
-// any math.  Per element the math is fp32 and independent of the geometry,
-// so any grid gives the same bits.
+// whose cost is launch geometry.  Here the grid is sized to the work (every
+// thread owns kVecPerThread 16-byte output vectors, all loads issued before
+// any math) rather than capped.  Per element the math is fp32 and independent
+// of the geometry, so any grid gives the same bits.
 #include <algorithm>
 
 #include "common.cuh"
@@ -32,9 +30,17 @@ __device__ __forceinline__ float exp_neg_abs(float g) {
     return y;
 }
 
+// 1 + t lies in (1, 2], where the hardware reciprocal (PTX ISA rcp.approx.f32)
+// is within one fp32 ulp; the bf16 result tolerates far more.
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ float silu_mul(float g, float u) {
     const float t = exp_neg_abs(g);
-    const float r = __frcp_rn(1.0f + t);
+    const float r = rcp_approx(1.0f + t);
     return g * (g >= 0.f ? r : t * r) * u;
 }
 
@@ -42,36 +48,42 @@ __device__ __forceinline__ uint32_t silu2(uint32_t g, uint32_t u) {
     return pack_bf16x2(silu_mul(bf16_lo(g), bf16_lo(u)), silu_mul(bf16_hi(g), bf16_hi(u)));
 }
 
-// Idx = uint32_t when M * d / 8 < 2^32 (cheap division), else uint64_t.
-template <typename Idx>
+// Thread t of the grid owns 16-byte output vectors t, t + S, t + 2S, ...
+// (S = all threads of the grid; consecutive threads take consecutive vectors,
+// so every warp access is one contiguous run).  The first vector's (row,
+// column) costs one division; each later one steps by (step_r, step_c) =
+// (S / nv, S mod nv) with a carry, so the loop has no division.
 __global__ void __launch_bounds__(kSiluThreads)
-silu_vec(uint16_t *__restrict__ out, const uint16_t *__restrict__ in, Idx total, Idx nv,
-         int64_t d) {
-    const Idx nthreads = static_cast<Idx>(gridDim.x) * kSiluThreads;
-    const Idx first = static_cast<Idx>(blockIdx.x) * kSiluThreads + threadIdx.x;
+silu_vec(uint16_t *__restrict__ out, const uint16_t *__restrict__ in, int64_t M, int64_t nv,
+         int64_t step_r, int64_t step_c, int64_t d) {
     pdl_wait();
     pdl_trigger();
-    for (Idx base = first; base < total; base += nthreads * kVecPerThread) {
-        uint4 g[kVecPerThread], u[kVecPerThread];
-        Idx idx[kVecPerThread];
+    const int64_t first = static_cast<int64_t>(blockIdx.x) * kSiluThreads + threadIdx.x;
+    int64_t r = first / nv, c = first - r * nv;
+    int64_t rr[kVecPerThread], cc[kVecPerThread];
+    uint4 g[kVecPerThread], u[kVecPerThread];
 #pragma unroll
-        for (int i = 0; i < kVecPerThread; ++i) {
-            idx[i] = base + nthreads * i;
-            if (idx[i] < total) {
-                const Idx r = idx[i] / nv, c = idx[i] - r * nv;
-                const uint16_t *gp = in + static_cast<int64_t>(r) * 2 * d + 8 * static_cast<int64_t>(c);
-                g[i] = ld_stream(gp);
-                u[i] = ld_stream(gp + d);
-            }
+    for (int i = 0; i < kVecPerThread; ++i) {
+        rr[i] = r;
+        cc[i] = c;
+        if (r < M) {
+            const uint16_t *gp = in + r * 2 * d + 8 * c;
+            g[i] = ld_stream(gp);
+            u[i] = ld_stream(gp + d);
         }
+        r += step_r;
+        c += step_c;
+        if (c >= nv) {
+            c -= nv;
+            ++r;
+        }
+    }
 #pragma unroll
-        for (int i = 0; i < kVecPerThread; ++i) {
-            if (idx[i] < total) {
-                const Idx r = idx[i] / nv, c = idx[i] - r * nv;
-                const uint4 o = make_uint4(silu2(g[i].x, u[i].x), silu2(g[i].y, u[i].y),
-                                           silu2(g[i].z, u[i].z), silu2(g[i].w, u[i].w));
-                st_vec(out + static_cast<int64_t>(r) * d + 8 * static_cast<int64_t>(c), o);
-            }
+    for (int i = 0; i < kVecPerThread; ++i) {
+        if (rr[i] < M) {
+            const uint4 o = make_uint4(silu2(g[i].x, u[i].x), silu2(g[i].y, u[i].y),
+                                       silu2(g[i].z, u[i].z), silu2(g[i].w, u[i].w));
+            st_vec(out + rr[i] * d + 8 * cc[i], o);
         }
     }
 }
@@ -120,15 +132,13 @@ extern "C" int silu_and_mul(void *out, const void *in, int64_t M, int64_t d,
     const bool vec_ok = aligned(in, 16) && aligned(out, 16) && d % 8 == 0;
     if (vec_ok) {
         const int64_t nv = d / 8, total = M * nv;
-        const int64_t grid = std::min<int64_t>(
-            ceil_div(ceil_div(total, kVecPerThread), kSiluThreads), 0x7FFFFFFF);
-        const dim3 g(static_cast<unsigned>(grid)), b(kSiluThreads);
+        const int64_t grid = ceil_div(ceil_div(total, kVecPerThread), kSiluThreads);
+        if (grid > 0x7FFFFFFF)
+            return GATED_ACT_ERR_TOO_LARGE;
+        const int64_t S = grid * kSiluThreads;
         const cudaError_t e =
-            total < (int64_t(1) << 32) - int64_t(grid) * kSiluThreads * kVecPerThread
-                ? launch_kernel(silu_vec<uint32_t>, g, b, 0, stream, 1, o, x,
-                                static_cast<uint32_t>(total), static_cast<uint32_t>(nv), d)
-                : launch_kernel(silu_vec<uint64_t>, g, b, 0, stream, 1, o, x,
-                                static_cast<uint64_t>(total), static_cast<uint64_t>(nv), d);
+            launch_kernel(silu_vec, dim3(static_cast<unsigned>(grid)), dim3(kSiluThreads), 0,
+                          stream, 1, o, x, M, nv, S / nv, S % nv, d);
         if (e != cudaSuccess)
             return cuda_status(e);
     } else {

@@ -90,6 +90,22 @@ int gelu_and_mul_sparse(void *out, const void *in, int64_t T, int64_t d,
 int silu_and_mul(void *out, const void *in, int64_t M, int64_t d,
                  cudaStream_t stream);
 
+/*
+ * Launch one empty kernel on `stream` with the same launch attributes as the
+ * activations (programmatic stream serialization, waiting for the preceding
+ * grid like they do).  For measuring launch overhead; no other effect.
+ */
+int gated_act_noop(cudaStream_t stream);
+
+/*
+ * Launch mode.  Every kernel is launched with programmatic stream
+ * serialization: it waits for the preceding grid in `stream` to complete and
+ * its writes to be visible before touching memory, and lets the next such
+ * launch in the stream begin early, so launch latency overlaps the previous
+ * kernel's tail.  Setting the environment variable GATED_ACT_PDL=0 before the
+ * first launch turns the attribute off (plain stream order).
+ */
+
 /* Human-readable text for a status code (static storage; never NULL). */
 const char *gated_act_status_string(int status);
 
