@@ -13,6 +13,8 @@ Inputs are bf16 bit patterns as ``numpy.uint16`` arrays.
       thresholding, tanh GELU, gated multiplication).
   silu_and_mul -- Megatron-LM PR "Size MoE activation kernel grid to the row
       count", section "What changed and why" (elementwise silu(gate) * up).
+  squared_relu -- same page, section "Scope and risks" (max(x, 0)^2).
+  gelu_and_mul -- the dense form of the sparse-GELU activation (no threshold).
 """
 from __future__ import annotations
 
@@ -71,6 +73,15 @@ class Oracle:
         lib.oracle_silu_and_mul.restype = ctypes.c_int
         lib.oracle_silu_and_mul.argtypes = [
             _c_u16_p, ctypes.c_int64, ctypes.c_int64, _c_double_p, _c_u16_p, ctypes.c_int]
+        lib.oracle_squared_relu.restype = ctypes.c_double
+        lib.oracle_squared_relu.argtypes = [ctypes.c_double]
+        lib.oracle_gelu_and_mul.restype = ctypes.c_int
+        lib.oracle_gelu_and_mul.argtypes = [
+            _c_u16_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, _c_double_p, _c_u16_p,
+            ctypes.c_int]
+        lib.oracle_squared_relu_rows.restype = ctypes.c_int
+        lib.oracle_squared_relu_rows.argtypes = [
+            _c_u16_p, ctypes.c_int64, ctypes.c_int64, _c_double_p, _c_u16_p, ctypes.c_int]
         self._lib = lib
 
     # -- scalar helpers -------------------------------------------------------
@@ -85,6 +96,9 @@ class Oracle:
 
     def silu(self, x: float) -> float:
         return self._lib.oracle_silu(float(x))
+
+    def squared_relu(self, x: float) -> float:
+        return self._lib.oracle_squared_relu(float(x))
 
     def max_threads(self) -> int:
         return int(self._lib.oracle_max_threads())
@@ -132,6 +146,38 @@ class Oracle:
                                            _ptr(ref16, _c_u16_p), int(nthreads))
         if rc != 0:
             raise ValueError(f"oracle_silu_and_mul rejected M={M} d={d}")
+        return ref, ref16
+
+
+    def gelu_and_mul(self, in_bits: np.ndarray, d: int, row_stride: int | None = None,
+                     nthreads: int = 0) -> tuple[np.ndarray, np.ndarray]:
+        """Dense gelu_tanh(g) * u on ``in_bits`` ([T, row_stride] uint16).
+
+        Returns (ref fp64 [T, d], ref rounded to bf16 bits uint16 [T, d]).
+        """
+        a = np.ascontiguousarray(in_bits, dtype=np.uint16)
+        T, rs = a.shape
+        if row_stride is not None and row_stride != rs:
+            raise ValueError("row_stride must equal the array's row length")
+        ref = np.empty((T, d), dtype=np.float64)
+        ref16 = np.empty((T, d), dtype=np.uint16)
+        rc = self._lib.oracle_gelu_and_mul(_ptr(a, _c_u16_p), T, d, rs, _ptr(ref, _c_double_p),
+                                           _ptr(ref16, _c_u16_p), int(nthreads))
+        if rc != 0:
+            raise ValueError(f"oracle_gelu_and_mul rejected T={T} d={d} rs={rs}")
+        return ref, ref16
+
+    def squared_relu_rows(self, in_bits: np.ndarray,
+                          nthreads: int = 0) -> tuple[np.ndarray, np.ndarray]:
+        """max(x, 0)^2 on ``in_bits`` ([M, d] uint16): (ref fp64, ref bf16 bits)."""
+        a = np.ascontiguousarray(in_bits, dtype=np.uint16)
+        M, d = a.shape
+        ref = np.empty((M, d), dtype=np.float64)
+        ref16 = np.empty((M, d), dtype=np.uint16)
+        rc = self._lib.oracle_squared_relu_rows(_ptr(a, _c_u16_p), M, d, _ptr(ref, _c_double_p),
+                                                _ptr(ref16, _c_u16_p), int(nthreads))
+        if rc != 0:
+            raise ValueError(f"oracle_squared_relu_rows rejected M={M} d={d}")
         return ref, ref16
 
 

@@ -26,7 +26,15 @@
  *  silu_and_mul -- Megatron-LM PR "Size MoE activation kernel grid to the row
  *      count", section "What changed and why": the elementwise MoE activation
  *      out_j = silu(g_j) * u_j with silu(x) = x / (1 + exp(-x)), gate in the
- *      first d columns and up in the next d.
+ *      first d columns and up in the next d.  The bounded form of the same
+ *      section (only the first n_rows live rows are computed) is this function
+ *      called on those rows.
+ *
+ *  squared_relu -- same page, section "Scope and risks": the sibling MoE
+ *      activation out_j = max(x_j, 0)^2 over [M, d] rows (not gated).
+ *
+ *  gelu_and_mul -- the dense form of the sparse-GELU page's activation (no
+ *      threshold): out_j = gelu_tanh(g_j) * u_j.
  *
  * Inputs are bf16 bit patterns (uint16), decoded exactly to double.  The
  * bf16 encoder below rounds a double to the nearest bf16, ties to even, in
@@ -83,11 +91,20 @@ uint16_t oracle_double_to_bf16(double v)
     return (uint16_t)(sign | (uint16_t)(w >> 16));
 }
 
-/* tanh-approximate GELU, in double with libm tanh. */
+/*
+ * tanh-approximate GELU, in double.  With y = sqrt(2/pi) (x + 0.044715 x^3),
+ * gelu_tanh(x) = 0.5 x (1 + tanh(y)).  For y < 0 the sum 1 + tanh(y) cancels,
+ * so that branch uses the exact identity 1 + tanh(y) = 2 e^{2y} / (1 + e^{2y}).
+ */
 double oracle_gelu_tanh(double x)
 {
     const double k = sqrt(2.0 / ORACLE_PI);
-    return 0.5 * x * (1.0 + tanh(k * (x + 0.044715 * x * x * x)));
+    const double y = k * (x + 0.044715 * x * x * x);
+    if (y < 0.0) {
+        const double t = exp(2.0 * y);
+        return x * t / (1.0 + t);
+    }
+    return 0.5 * x * (1.0 + tanh(y));
 }
 
 /* SiLU (swish), in double with libm exp. */
@@ -170,6 +187,64 @@ int oracle_gelu_and_mul_sparse(const uint16_t *in, int64_t T, int64_t d,
             row_std[r] = std;
         if (row_cutoff)
             row_cutoff[r] = cutoff;
+    }
+    return 0;
+}
+
+/* squared ReLU, in double. */
+double oracle_squared_relu(double x)
+{
+    double r = x > 0.0 ? x : 0.0;
+    if (isnan(x))
+        r = x;
+    return r * r;
+}
+
+/*
+ * gelu_and_mul (dense): out = gelu_tanh(g) * u on [T, row_stride] rows.
+ *   ref      : T*d doubles (may be NULL);  ref_bf16 : T*d bf16 patterns (may be NULL)
+ */
+int oracle_gelu_and_mul(const uint16_t *in, int64_t T, int64_t d, int64_t row_stride,
+                        double *ref, uint16_t *ref_bf16, int nthreads)
+{
+    if (T < 0 || d <= 0 || row_stride < 2 * d)
+        return -1;
+    set_threads(nthreads);
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < T; ++r) {
+        const uint16_t *gate = in + r * row_stride;
+        const uint16_t *up = gate + d;
+        for (int64_t j = 0; j < d; ++j) {
+            double y = oracle_gelu_tanh(oracle_bf16_to_double(gate[j])) *
+                       oracle_bf16_to_double(up[j]);
+            if (ref)
+                ref[r * d + j] = y;
+            if (ref_bf16)
+                ref_bf16[r * d + j] = oracle_double_to_bf16(y);
+        }
+    }
+    return 0;
+}
+
+/*
+ * squared_relu over a contiguous [M, d] bf16 input.
+ *   ref : M*d doubles (may be NULL);  ref_bf16 : M*d bf16 patterns (may be NULL)
+ */
+int oracle_squared_relu_rows(const uint16_t *in, int64_t M, int64_t d, double *ref,
+                             uint16_t *ref_bf16, int nthreads)
+{
+    if (M < 0 || d <= 0)
+        return -1;
+    set_threads(nthreads);
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < M; ++r) {
+        for (int64_t j = 0; j < d; ++j) {
+            double y = oracle_squared_relu(oracle_bf16_to_double(in[r * d + j]));
+            if (ref)
+                ref[r * d + j] = y;
+            if (ref_bf16)
+                ref_bf16[r * d + j] = oracle_double_to_bf16(y);
+        }
     }
     return 0;
 }

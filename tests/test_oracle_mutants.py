@@ -39,6 +39,20 @@ MUTANTS = {
     "encode_via_float": ("double r = rint(a / q) * q;",
                          "double r = rint((double)(float)a / q) * q;"),
     "silu_sign": ("return x / (1.0 + exp(-x));", "return x / (1.0 + exp(x));"),
+    "gelu_negative_branch": ("return x * t / (1.0 + t);", "return x * t / (1.0 - t);"),
+    "gelu_negative_exponent": ("const double t = exp(2.0 * y);", "const double t = exp(y);"),
+    "squared_relu_not_squared": ("    return r * r;", "    return r;"),
+    "squared_relu_keeps_negative": ("double r = x > 0.0 ? x : 0.0;", "double r = x;"),
+    "dense_gelu_uses_up_twice": ("double y = oracle_gelu_tanh(oracle_bf16_to_double(gate[j])) *\n"
+                                 "                       oracle_bf16_to_double(up[j]);\n"
+                                 "            if (ref)\n                ref[r * d + j] = y;\n"
+                                 "            if (ref_bf16)\n                ref_bf16[r * d + j] = oracle_double_to_bf16(y);\n"
+                                 "        }\n    }\n    return 0;\n}\n\n/*\n * squared_relu",
+                                 "double y = oracle_gelu_tanh(oracle_bf16_to_double(up[j])) *\n"
+                                 "                       oracle_bf16_to_double(up[j]);\n"
+                                 "            if (ref)\n                ref[r * d + j] = y;\n"
+                                 "            if (ref_bf16)\n                ref_bf16[r * d + j] = oracle_double_to_bf16(y);\n"
+                                 "        }\n    }\n    return 0;\n}\n\n/*\n * squared_relu"),
     "silu_up_is_gate": ("double y = oracle_silu(oracle_bf16_to_double(gate[j])) *\n"
                         "                       oracle_bf16_to_double(up[j]);",
                         "double y = oracle_silu(oracle_bf16_to_double(gate[j])) *\n"
@@ -85,6 +99,18 @@ def _battery(o: O.Oracle) -> dict:
     sf = s.to(torch.float64)
     out["silu_and_mul_vs_torch"] = bool(np.allclose(r64, (F.silu(sf[:, :32]) * sf[:, 32:]).numpy(),
                                                     rtol=1e-13, atol=1e-300))
+    xs = np.linspace(-9, 3, 97)
+    out["gelu_negative_tail"] = bool(np.allclose(
+        [o.gelu_tanh(x) for x in xs],
+        F.gelu(torch.tensor(xs), approximate="tanh").numpy(), rtol=1e-10, atol=1e-13))
+    dx = W.iid(5, 24, seed=6).x
+    g64, _ = o.gelu_and_mul(W.to_bits(dx), d=24)
+    dxf = dx.to(torch.float64)
+    out["dense_gelu_vs_torch"] = bool(np.allclose(
+        g64, (F.gelu(dxf[:, :24], approximate="tanh") * dxf[:, 24:]).numpy(), rtol=1e-12,
+        atol=1e-15))
+    q64, _ = o.squared_relu_rows(W.to_bits(dx))
+    out["squared_relu_vs_torch"] = bool(np.array_equal(q64, (torch.relu(dxf) ** 2).numpy()))
     out["silu_rounded"] = bool(np.all(
         np.abs(W.from_bits(r16).to(torch.float64).numpy() - r64) <= np.abs(r64) * 2.0 ** -8 + 1e-38))
     return out
