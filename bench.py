@@ -81,6 +81,24 @@ def workload_launches(only: tuple | None = None) -> list[dict]:
     return out
 
 
+def extra_launches() -> list[dict]:
+    """Widened rows, measured per shape (not part of the timed step): the
+    bounded silu at the MoE page's case (a 16384-row buffer bound with 2048
+    live rows, and fully live), dense gelu_and_mul and squared_relu."""
+    import workloads as W
+    d = W.SILU_D
+    return [
+        {"op": "silu_bounded", "T": 16384, "d": d, "live": 2048, "z": None,
+         "bytes": silu_bytes(2048, d)},
+        {"op": "silu_bounded", "T": 16384, "d": d, "live": 16384, "z": None,
+         "bytes": silu_bytes(16384, d)},
+        {"op": "gelu_dense", "T": 2048, "d": 16384, "z": None, "bytes": gelu_bytes(2048, 16384)},
+        {"op": "gelu_dense", "T": 64, "d": 8192, "z": None, "bytes": gelu_bytes(64, 8192)},
+        {"op": "squared_relu", "T": 2048, "d": d, "z": None, "bytes": 2048 * d * 2 * 2},
+        {"op": "squared_relu", "T": 16384, "d": d, "z": None, "bytes": 16384 * d * 2 * 2},
+    ]
+
+
 def load_peaks() -> dict:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -250,10 +268,23 @@ def kernel_name(plan: dict) -> str:
 
 # ----------------------------------------------------------------- our arm
 def _launch(ga, L, x, out):
-    if L["op"] == "gelu":
+    op = L["op"]
+    if op == "gelu":
         ga.gelu_and_mul_sparse(x, L["z"], d=L["d"], out=out)
-    else:
+    elif op == "silu":
         ga.silu_and_mul(x, out=out)
+    elif op == "silu_bounded":
+        ga.silu_and_mul_bounded(x, L["n_rows"], out=out)
+    elif op == "gelu_dense":
+        ga.gelu_and_mul(x, d=L["d"], out=out)
+    elif op == "squared_relu":
+        ga.squared_relu(x, out=out)
+    else:
+        raise ValueError(op)
+
+
+def _in_width(L) -> int:
+    return L["d"] if L["op"] == "squared_relu" else 2 * L["d"]
 
 
 def per_shape_times(ga, launches, dev, peak_gbs, reps=5) -> tuple[list, float]:
@@ -291,28 +322,42 @@ def per_shape_times(ga, launches, dev, peak_gbs, reps=5) -> tuple[list, float]:
     rows = []
     seen = {}
     for L in launches:
-        key = (L["op"], L["T"], L["d"], L["z"])
+        key = (L["op"], L["T"], L["d"], L["z"], L.get("live"))
         if key in seen:
             continue
         T, d = L["T"], L["d"]
-        n_in, n_out = T * 2 * d, T * d
+        if L["op"] == "silu_bounded":
+            L["n_rows"] = torch.tensor([L["live"]], dtype=torch.int32, device=dev)
+        n_in, n_out = T * _in_width(L), T * d
         win = max(1, min(arena_in.numel() // n_in, arena_out.numel() // n_out))
         N = int(min(200, max(20, win)))
         fns = []
         for i in range(N):
             w = i % win
-            x = arena_in[w * n_in:(w + 1) * n_in].view(T, 2 * d)
+            x = arena_in[w * n_in:(w + 1) * n_in].view(T, _in_width(L))
             o = arena_out[w * n_out:(w + 1) * n_out].view(T, d)
             fns.append(lambda x=x, o=o, L=L: _launch(ga, L, x, o))
         t = timed_graph(fns)
         seen[key] = t
         gbs = L["bytes"] / (t * 1e-3) / 1e9
         floor = floor_ms + L["bytes"] / (peak_gbs * 1e9) * 1e3
-        rows.append({"op": L["op"], "T": T, "d": d, "z": L["z"], "kernel": L["kernel"],
-                     "us": round(t * 1e3, 3), "GBps": round(gbs, 1),
-                     "frac_of_measured": round(gbs / peak_gbs, 4),
-                     "frac_of_spec_8TBps": round(gbs / SPEC_HBM_GBS, 4),
-                     "x_floor": round(t / floor, 3), "launches_in_graph": N})
+        row = {"op": L["op"], "T": T, "d": d, "z": L["z"], "kernel": L.get("kernel", L["op"]),
+               "us": round(t * 1e3, 3), "GBps": round(gbs, 1),
+               "frac_of_measured": round(gbs / peak_gbs, 4),
+               "frac_of_spec_8TBps": round(gbs / SPEC_HBM_GBS, 4),
+               "x_floor": round(t / floor, 3), "launches_in_graph": N}
+        if "live" in L:
+            row["live_rows"] = L["live"]
+        if L["op"] == "gelu" and T <= 64:
+            # the same bytes through a purely elementwise kernel (dense
+            # gelu_and_mul: no reduction): what streaming these rows costs
+            sfns = [lambda x=arena_in[(i % win) * n_in:((i % win) + 1) * n_in].view(T, 2 * d),
+                    o=arena_out[(i % win) * n_out:((i % win) + 1) * n_out].view(T, d):
+                    ga.gelu_and_mul(x, d=d, out=o) for i in range(N)]
+            ts = timed_graph(sfns)
+            row["stream_us"] = round(ts * 1e3, 3)
+            row["x_stream"] = round(t / ts, 3)
+        rows.append(row)
     del arena_in, arena_out
     torch.cuda.synchronize()
     return rows, floor_ms * 1e3
@@ -349,14 +394,17 @@ def run_ours(args, world, rank, local):
         _launch(ga, L, dev_in[i], dev_out[i])
     torch.cuda.synchronize()
 
-    shapes, floor_us = per_shape_times(ga, launches, dev, peaks["hbm_gbs"]) \
+    shapes, floor_us = per_shape_times(ga, launches + ([] if args.only else extra_launches()),
+                                       dev, peaks["hbm_gbs"]) \
         if not args.no_per_shape else ([], None)
+    shapes_step = [r for r in shapes if r["op"] in ("gelu", "silu")]
+    widened = [r for r in shapes if r["op"] not in ("gelu", "silu")]
 
     # the dominant kernel (largest total time per step, from the per-shape table
     # when present, else from bytes) runs as graph A, everything else as graph B
     def weight(i, L):
-        if shapes:
-            for r in shapes:
+        if shapes_step:
+            for r in shapes_step:
                 if (r["op"], r["T"], r["d"], r["z"]) == (L["op"], L["T"], L["d"], L["z"]):
                     return r["us"]
         return L["bytes"]
@@ -443,7 +491,7 @@ def run_ours(args, world, rank, local):
                        "parallelism": f"rows sharded over {world} GPU(s), no collective",
                        "launch_floor_us": None if floor_us is None else round(floor_us, 3)},
             "roofline": roofline, "e2e": e2e, "gpu_launches": len(launches) * args.steps,
-            "clocks": clk.summary(), "per_shape": shapes}
+            "clocks": clk.summary(), "per_shape": shapes_step, "widened_rows": widened}
     if cpu is not None:
         line["cpu_baseline"] = cpu
     if rank == 0:

@@ -28,7 +28,8 @@ VARIANT_NAMES = {0: "auto", 1: "warp_rows", 2: "cta_row", 3: "scalar", 4: "tma_r
 EXPORTED = (
     "gelu_and_mul_sparse", "silu_and_mul", "gated_act_status_string",
     "gated_act_last_cuda_error", "gelu_and_mul_sparse_plan", "gelu_and_mul_sparse_ex",
-    "gated_act_device_status", "gated_act_noop",
+    "gated_act_device_status", "gated_act_noop", "silu_and_mul_bounded", "gelu_and_mul",
+    "squared_relu",
 )
 
 
@@ -88,6 +89,12 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.gated_act_device_status.restype = ctypes.c_int
     lib.gated_act_noop.argtypes = [vp]
     lib.gated_act_noop.restype = ctypes.c_int
+    lib.silu_and_mul_bounded.argtypes = [vp, cvp, i64, i64, cvp, vp]
+    lib.silu_and_mul_bounded.restype = ctypes.c_int
+    lib.gelu_and_mul.argtypes = [vp, cvp, i64, i64, i64, vp]
+    lib.gelu_and_mul.restype = ctypes.c_int
+    lib.squared_relu.argtypes = [vp, cvp, i64, i64, vp]
+    lib.squared_relu.restype = ctypes.c_int
     if path is None:
         _lib = lib
     return lib
@@ -195,6 +202,65 @@ def silu_and_mul(x: torch.Tensor, out: torch.Tensor | None = None,
     return out
 
 
-__all__ = ["gelu_and_mul_sparse", "gelu_and_mul_sparse_plan", "silu_and_mul", "device_status", "noop",
+def _gated_in(x: torch.Tensor, d: int | None) -> tuple[int, int, int]:
+    T, rs = _rows_view(x)
+    if d is None:
+        if x.shape[1] % 2:
+            raise ValueError("odd row length: pass d explicitly")
+        d = int(x.shape[1]) // 2
+    if x.shape[1] < 2 * d:
+        raise ValueError("rows are shorter than 2d")
+    return T, rs, d
+
+
+def _out_for(out: torch.Tensor | None, T: int, d: int, device) -> torch.Tensor:
+    if out is None:
+        return torch.empty((T, d), dtype=torch.bfloat16, device=device)
+    if out.shape != (T, d) or out.dtype != torch.bfloat16 or not out.is_contiguous():
+        raise ValueError(f"out must be a contiguous [{T}, {d}] bf16 tensor")
+    return out
+
+
+def silu_and_mul_bounded(x: torch.Tensor, n_rows: torch.Tensor, out: torch.Tensor | None = None,
+                         stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """silu_and_mul over the first ``n_rows`` rows (a 1-element int32 CUDA tensor).
+
+    Rows at or past the live count are left untouched in ``out``.
+    """
+    if x.dim() != 2 or x.dtype != torch.bfloat16 or not x.is_cuda or not x.is_contiguous():
+        raise ValueError("input must be a contiguous 2-D bf16 CUDA tensor [M, 2d]")
+    if n_rows.dtype != torch.int32 or not n_rows.is_cuda or n_rows.numel() < 1:
+        raise ValueError("n_rows must be an int32 CUDA tensor")
+    M, d = int(x.shape[0]), int(x.shape[1]) // 2
+    out = _out_for(out, M, d, x.device)
+    rc = load_library().silu_and_mul_bounded(out.data_ptr(), x.data_ptr(), M, d,
+                                             n_rows.data_ptr(), _stream_handle(stream))
+    _check("silu_and_mul_bounded", rc)
+    return out
+
+
+def gelu_and_mul(x: torch.Tensor, d: int | None = None, out: torch.Tensor | None = None,
+                 stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """Dense gelu_tanh(gate) * up of ``x`` ([T, >=2d] bf16 CUDA): returns [T, d] bf16."""
+    T, rs, d = _gated_in(x, d)
+    out = _out_for(out, T, d, x.device)
+    rc = load_library().gelu_and_mul(out.data_ptr(), x.data_ptr(), T, d, rs, _stream_handle(stream))
+    _check("gelu_and_mul", rc)
+    return out
+
+
+def squared_relu(x: torch.Tensor, out: torch.Tensor | None = None,
+                 stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """max(x, 0)^2 of a contiguous [M, d] bf16 CUDA tensor."""
+    if x.dim() != 2 or x.dtype != torch.bfloat16 or not x.is_cuda or not x.is_contiguous():
+        raise ValueError("input must be a contiguous 2-D bf16 CUDA tensor [M, d]")
+    M, d = int(x.shape[0]), int(x.shape[1])
+    out = _out_for(out, M, d, x.device)
+    rc = load_library().squared_relu(out.data_ptr(), x.data_ptr(), M, d, _stream_handle(stream))
+    _check("squared_relu", rc)
+    return out
+
+
+__all__ = ["silu_and_mul_bounded", "gelu_and_mul", "squared_relu", "gelu_and_mul_sparse", "gelu_and_mul_sparse_plan", "silu_and_mul", "device_status", "noop",
            "load_library",
            "status_string", "GatedActError", "Plan", "EXPORTED", "LIB_PATH"]

@@ -21,7 +21,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIB_DIR, "libgated_act.so")
-SOURCES = ("api.cu", "gelu_and_mul_sparse.cu", "silu_and_mul.cu")
+SOURCES = ("api.cu", "gelu_and_mul_sparse.cu", "elementwise.cu")
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
 

@@ -1,7 +1,8 @@
 /*
  * gated_act.h -- C ABI of the GB300 (sm_103a) fused gated-activation library.
  *
- * Two operations over bf16 activations, each one kernel launch:
+ * Fused activations over bf16 rows, each one kernel launch.  The two the
+ * library is built around:
  *
  *   gelu_and_mul_sparse  Gemma3n's sparse GELU gate.  vLLM PR "[Performance]
  *       Add Triton kernel for Gemma3n sparse GELU", section "Purpose": per-row
@@ -105,6 +106,42 @@ int gated_act_noop(cudaStream_t stream);
  * kernel's tail.  Setting the environment variable GATED_ACT_PDL=0 before the
  * first launch turns the attribute off (plain stream order).
  */
+
+/*
+ * silu_and_mul_bounded -- silu_and_mul over the live rows only.
+ * Megatron-LM PR "Size MoE activation kernel grid to the row count", section
+ * "What changed and why": under CUDA graphs the grid is fixed by the
+ * capture-time bound M while the number of live MoE rows changes per step;
+ * the live count is read on the device, and CTAs past it exit early.
+ *   out, in, M, d  as silu_and_mul (M is the buffer bound).
+ *   n_rows         DEVICE pointer to one int32, the live row count, read by
+ *                  the kernel after the preceding work in `stream`; clamped to
+ *                  [0, M].  Output rows >= the live count are not written.
+ * The launch depends only on M and d, so one capture serves every count.
+ */
+int silu_and_mul_bounded(void *out, const void *in, int64_t M, int64_t d,
+                         const int32_t *n_rows, cudaStream_t stream);
+
+/*
+ * gelu_and_mul -- the dense form of the sparse-GELU activation (no
+ * threshold): out = gelu_tanh(gate) * up, fp32 math, bf16 out.
+ *   out  [T, d] bf16 contiguous;  in [T, row_stride] bf16, gate = [0, d),
+ *   up = [d, 2d), row_stride >= 2d.
+ * Accuracy: within one bf16 ulp of the correctly rounded result.
+ */
+int gelu_and_mul(void *out, const void *in, int64_t T, int64_t d,
+                 int64_t row_stride, cudaStream_t stream);
+
+/*
+ * squared_relu -- out = max(x, 0)^2 elementwise, not gated (the sibling MoE
+ * activation in Megatron-LM PR "Size MoE activation kernel grid to the row
+ * count", section "Scope and risks").
+ *   out [M, d] bf16 contiguous;  in [M, d] bf16 contiguous; no overlap.
+ * Exact: x^2 of a bf16 value is exact in fp32, so the output is the correctly
+ * rounded bf16 of max(x, 0)^2.
+ */
+int squared_relu(void *out, const void *in, int64_t M, int64_t d,
+                 cudaStream_t stream);
 
 /* Human-readable text for a status code (static storage; never NULL). */
 const char *gated_act_status_string(int status);

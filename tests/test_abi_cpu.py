@@ -93,6 +93,23 @@ def test_silu_rejects_null_odd_and_overlap(lib):
     assert lib.silu_and_mul(0x100000 + 100, 0x100000, 4, 8, None) == ga.ERR_OVERLAP
 
 
+def test_widened_rows_reject_bad_arguments(lib):
+    # silu_and_mul_bounded needs a live-count pointer, aligned to 4
+    assert lib.silu_and_mul_bounded(0x1000, 0x100000, 4, 8, None, None) == ga.ERR_NULL
+    assert lib.silu_and_mul_bounded(0x1000, 0x100000, 4, 8, 0x2002, None) == ga.ERR_ALIGN
+    assert lib.silu_and_mul_bounded(0x1000, 0x100000, -1, 8, 0x2000, None) == ga.ERR_SIZE
+    assert lib.silu_and_mul_bounded(None, None, 0, 8, None, None) == ga.OK
+    # gelu_and_mul takes a row stride
+    assert lib.gelu_and_mul(0x1000, 0x100000, 4, 8, 15, None) == ga.ERR_STRIDE
+    assert lib.gelu_and_mul(0x1000, 0x100000, 4, 0, 16, None) == ga.ERR_SIZE
+    assert lib.gelu_and_mul(0x100000 + 8, 0x100000, 4, 8, 16, None) == ga.ERR_OVERLAP
+    assert lib.gelu_and_mul(None, None, 0, 8, 16, None) == ga.OK
+    # squared_relu is not gated: [M, d] -> [M, d]
+    assert lib.squared_relu(0x1000, 0x100000, 4, 0, None) == ga.ERR_SIZE
+    assert lib.squared_relu(None, 0x100000, 4, 8, None) == ga.ERR_NULL
+    assert lib.squared_relu(0x100000 + 62, 0x100000, 4, 8, None) == ga.ERR_OVERLAP
+
+
 def plan(lib, T, d, rs=None, variant=0, cluster=0, sms=GB300_SMS, out=0x10000, inp=0x100000):
     p = ga.Plan()
     rc = lib.gelu_and_mul_sparse_plan(out, inp, T, d, rs or 2 * d, variant, cluster, sms,
