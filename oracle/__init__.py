@@ -73,6 +73,13 @@ class Oracle:
         lib.oracle_silu_and_mul.restype = ctypes.c_int
         lib.oracle_silu_and_mul.argtypes = [
             _c_u16_p, ctypes.c_int64, ctypes.c_int64, _c_double_p, _c_u16_p, ctypes.c_int]
+        lib.oracle_f16_to_double.restype = ctypes.c_double
+        lib.oracle_f16_to_double.argtypes = [ctypes.c_uint16]
+        lib.oracle_gelu_and_mul_sparse_typed.restype = ctypes.c_int
+        lib.oracle_gelu_and_mul_sparse_typed.argtypes = [
+            ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+            ctypes.c_double, _c_double_p, _c_u8_p, _c_double_p, _c_double_p, _c_double_p,
+            ctypes.c_int]
         lib.oracle_squared_relu.restype = ctypes.c_double
         lib.oracle_squared_relu.argtypes = [ctypes.c_double]
         lib.oracle_gelu_and_mul.restype = ctypes.c_int
@@ -90,6 +97,9 @@ class Oracle:
 
     def double_to_bf16(self, v: float) -> int:
         return int(self._lib.oracle_double_to_bf16(float(v)))
+
+    def f16_to_double(self, bits: int) -> float:
+        return self._lib.oracle_f16_to_double(int(bits) & 0xFFFF)
 
     def gelu_tanh(self, x: float) -> float:
         return self._lib.oracle_gelu_tanh(float(x))
@@ -125,6 +135,35 @@ class Oracle:
             _ptr(cutoff, _c_double_p), int(nthreads))
         if rc != 0:
             raise ValueError(f"oracle_gelu_and_mul_sparse rejected T={T} d={d} rs={rs}")
+        return GeluSparseResult(ref, mask.astype(bool), mean, std, cutoff)
+
+    def gelu_and_mul_sparse_typed(self, x: np.ndarray, d: int, z: float,
+                                  bf16_bits: bool = False, nthreads: int = 0) -> GeluSparseResult:
+        """gelu_and_mul_sparse on a [T, row_stride] numpy array of float16 or
+        float32 values, or of bf16 bit patterns (uint16 with bf16_bits=True)."""
+        a = np.ascontiguousarray(x)
+        if a.dtype == np.uint16:
+            if not bf16_bits:
+                raise ValueError("uint16 input must be bf16 bit patterns (bf16_bits=True)")
+            code = 0
+        elif a.dtype == np.float16:
+            code = 1
+        elif a.dtype == np.float32:
+            code = 2
+        else:
+            raise ValueError(f"unsupported element type {a.dtype}")
+        T, rs = a.shape
+        ref = np.empty((T, d), dtype=np.float64)
+        mask = np.empty((T, d), dtype=np.uint8)
+        mean = np.empty(T, dtype=np.float64)
+        std = np.empty(T, dtype=np.float64)
+        cutoff = np.empty(T, dtype=np.float64)
+        rc = self._lib.oracle_gelu_and_mul_sparse_typed(
+            a.ctypes.data_as(ctypes.c_void_p), code, T, d, rs, float(z), _ptr(ref, _c_double_p),
+            _ptr(mask, _c_u8_p), _ptr(mean, _c_double_p), _ptr(std, _c_double_p),
+            _ptr(cutoff, _c_double_p), int(nthreads))
+        if rc != 0:
+            raise ValueError(f"oracle_gelu_and_mul_sparse_typed rejected T={T} d={d} rs={rs}")
         return GeluSparseResult(ref, mask.astype(bool), mean, std, cutoff)
 
     def silu_and_mul(self, in_bits: np.ndarray, d: int | None = None,

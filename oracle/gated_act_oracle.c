@@ -36,9 +36,10 @@
  *  gelu_and_mul -- the dense form of the sparse-GELU page's activation (no
  *      threshold): out_j = gelu_tanh(g_j) * u_j.
  *
- * Inputs are bf16 bit patterns (uint16), decoded exactly to double.  The
- * bf16 encoder below rounds a double to the nearest bf16, ties to even, in
- * one step (no detour through float, which would round twice).
+ * Inputs are bf16 bit patterns (uint16), decoded exactly to double; the
+ * sparse GELU also takes fp16 and fp32 elements (the page validates all three
+ * types).  The bf16 encoder below rounds a double to the nearest bf16, ties
+ * to even, in one step (no detour through float, which would round twice).
  */
 #include <math.h>
 #include <stdint.h>
@@ -49,6 +50,27 @@
 #endif
 
 #define ORACLE_PI 3.14159265358979323846
+
+/* Element types of the typed entry points (same numbering as the library's). */
+enum { ORACLE_BF16 = 0, ORACLE_F16 = 1, ORACLE_F32 = 2 };
+
+/*
+ * Exact value of an IEEE binary16 bit pattern: sign, 5 exponent bits (bias
+ * 15), 10 fraction bits; exponent 0 is subnormal (fraction * 2^-24), 31 is
+ * infinity (fraction 0) or NaN.
+ */
+double oracle_f16_to_double(uint16_t bits)
+{
+    const int sign = bits >> 15, e = (bits >> 10) & 0x1F, f = bits & 0x3FF;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -24);
+    else if (e == 31)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexp((double)(f + 1024), e - 25);
+    return sign ? -v : v;
+}
 
 /* Exact value of a bf16 bit pattern: the top 16 bits of an IEEE binary32. */
 double oracle_bf16_to_double(uint16_t bits)
@@ -89,6 +111,19 @@ uint16_t oracle_double_to_bf16(double v)
     uint32_t w;
     memcpy(&w, &f, sizeof w);
     return (uint16_t)(sign | (uint16_t)(w >> 16));
+}
+
+/* Element j of a typed array, exactly, in double. */
+static double load_elem(const void *base, int dtype, int64_t j)
+{
+    if (dtype == ORACLE_F32) {
+        float f;
+        memcpy(&f, (const char *)base + 4 * j, sizeof f);
+        return (double)f;
+    }
+    uint16_t b;
+    memcpy(&b, (const char *)base + 2 * j, sizeof b);
+    return dtype == ORACLE_F16 ? oracle_f16_to_double(b) : oracle_bf16_to_double(b);
 }
 
 /*
@@ -134,36 +169,34 @@ int oracle_max_threads(void)
 }
 
 /*
- * gelu_and_mul_sparse, one row at a time.
- *   in         : T rows of row_stride bf16 values; gate = [0,d), up = [d,2d)
+ * gelu_and_mul_sparse, one row at a time, on elements of type `dtype`.
+ *   in         : T rows of row_stride elements; gate = [0,d), up = [d,2d)
  *   ref        : T*d doubles, the unrounded result
  *   mask       : T*d bytes, 1 where g_j > cutoff (strictly), else 0
  *   row_mean, row_std, row_cutoff : T doubles each (any may be NULL)
  *   nthreads   : OpenMP threads over rows (<= 0: the runtime default)
- * Returns 0, or -1 on a bad size.
+ * Returns 0, or -1 on a bad size or type.
  */
-int oracle_gelu_and_mul_sparse(const uint16_t *in, int64_t T, int64_t d,
-                               int64_t row_stride, double z, double *ref,
-                               uint8_t *mask, double *row_mean,
-                               double *row_std, double *row_cutoff,
-                               int nthreads)
+int oracle_gelu_and_mul_sparse_typed(const void *in, int dtype, int64_t T, int64_t d,
+                                     int64_t row_stride, double z, double *ref,
+                                     uint8_t *mask, double *row_mean, double *row_std,
+                                     double *row_cutoff, int nthreads)
 {
-    if (T < 0 || d <= 0 || row_stride < 2 * d)
+    if (T < 0 || d <= 0 || row_stride < 2 * d || dtype < ORACLE_BF16 || dtype > ORACLE_F32)
         return -1;
     set_threads(nthreads);
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t r = 0; r < T; ++r) {
-        const uint16_t *gate = in + r * row_stride;
-        const uint16_t *up = gate + d;
+        const int64_t g0 = r * row_stride, u0 = g0 + d;
 
         double sum = 0.0;
         for (int64_t j = 0; j < d; ++j)
-            sum += oracle_bf16_to_double(gate[j]);
+            sum += load_elem(in, dtype, g0 + j);
         double mean = sum / (double)d;
 
         double ss = 0.0;
         for (int64_t j = 0; j < d; ++j) {
-            double dev = oracle_bf16_to_double(gate[j]) - mean;
+            double dev = load_elem(in, dtype, g0 + j) - mean;
             ss += dev * dev;
         }
         double var = ss / (double)d;
@@ -172,8 +205,8 @@ int oracle_gelu_and_mul_sparse(const uint16_t *in, int64_t T, int64_t d,
         double cutoff = mean + std * z;
 
         for (int64_t j = 0; j < d; ++j) {
-            double g = oracle_bf16_to_double(gate[j]);
-            double u = oracle_bf16_to_double(up[j]);
+            double g = load_elem(in, dtype, g0 + j);
+            double u = load_elem(in, dtype, u0 + j);
             double s = g - cutoff;
             if (s < 0.0)
                 s = 0.0;
@@ -189,6 +222,17 @@ int oracle_gelu_and_mul_sparse(const uint16_t *in, int64_t T, int64_t d,
             row_cutoff[r] = cutoff;
     }
     return 0;
+}
+
+/* gelu_and_mul_sparse on bf16 bit patterns (the library's default type). */
+int oracle_gelu_and_mul_sparse(const uint16_t *in, int64_t T, int64_t d,
+                               int64_t row_stride, double z, double *ref,
+                               uint8_t *mask, double *row_mean,
+                               double *row_std, double *row_cutoff,
+                               int nthreads)
+{
+    return oracle_gelu_and_mul_sparse_typed(in, ORACLE_BF16, T, d, row_stride, z, ref, mask,
+                                            row_mean, row_std, row_cutoff, nthreads);
 }
 
 /* squared ReLU, in double. */

@@ -33,8 +33,12 @@ MUTANTS = {
     "gelu_unshifted": ("ref[r * d + j] = oracle_gelu_tanh(s) * u;",
                        "ref[r * d + j] = (s > 0.0 ? oracle_gelu_tanh(g) : 0.0) * u;"),
     "mask_not_strict": ("(uint8_t)(g > cutoff)", "(uint8_t)(g >= cutoff)"),
-    "up_offset": ("const uint16_t *up = gate + d;\n\n        double sum",
-                  "const uint16_t *up = gate + d - 1;\n\n        double sum"),
+    "up_offset": ("const int64_t g0 = r * row_stride, u0 = g0 + d;",
+                  "const int64_t g0 = r * row_stride, u0 = g0 + d - 1;"),
+    "f16_exponent_bias": ("v = ldexp((double)(f + 1024), e - 25);",
+                          "v = ldexp((double)(f + 1024), e - 24);"),
+    "f16_subnormal_scale": ("v = ldexp((double)f, -24);", "v = ldexp((double)f, -25);"),
+    "f32_read_as_f16": ("    if (dtype == ORACLE_F32) {", "    if (dtype == -1) {"),
     "encode_truncates": ("double r = rint(a / q) * q;", "double r = floor(a / q) * q;"),
     "encode_via_float": ("double r = rint(a / q) * q;",
                          "double r = rint((double)(float)a / q) * q;"),
@@ -111,6 +115,16 @@ def _battery(o: O.Oracle) -> dict:
         atol=1e-15))
     q64, _ = o.squared_relu_rows(W.to_bits(dx))
     out["squared_relu_vs_torch"] = bool(np.array_equal(q64, (torch.relu(dxf) ** 2).numpy()))
+    hb = np.arange(0, 1 << 16, 64, dtype=np.uint32).astype(np.uint16)
+    hv = hb.view(np.float16).astype(np.float64)
+    hg = np.array([o.f16_to_double(int(b)) for b in hb])
+    fin = np.isfinite(hv)
+    out["f16_decode_vs_numpy"] = bool(np.array_equal(hg[fin], hv[fin]))
+    x32 = (np.random.default_rng(2).standard_normal((3, 80)) * 2).astype(np.float32)
+    t32 = o.gelu_and_mul_sparse_typed(x32, d=40, z=0.4)
+    out["typed_f32_vs_torch"] = bool(np.allclose(
+        t32.ref, _composition(torch.from_numpy(x32.astype(np.float64)), 40, 0.4).numpy(),
+        rtol=1e-12, atol=1e-13))
     out["silu_rounded"] = bool(np.all(
         np.abs(W.from_bits(r16).to(torch.float64).numpy() - r64) <= np.abs(r64) * 2.0 ** -8 + 1e-38))
     return out

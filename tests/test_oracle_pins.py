@@ -339,3 +339,41 @@ def test_squared_relu_against_library_exactly(oracle):
     assert np.array_equal(ref16, t16)
     assert oracle.squared_relu(-0.5) == 0.0 and oracle.squared_relu(3.0) == 9.0
     assert np.isnan(oracle.squared_relu(float("nan")))
+
+
+# ---------------------------------------------------------------- fp16 / fp32 elements
+def test_f16_decode_matches_numpy_for_all_patterns(oracle):
+    bits = np.arange(0, 1 << 16, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = np.array([oracle.f16_to_double(int(b)) for b in bits])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert oracle.f16_to_double(0x0001) == 2.0 ** -24 and oracle.f16_to_double(0x7BFF) == 65504.0
+
+
+@pytest.mark.parametrize("dt", [np.float16, np.float32])
+def test_typed_sparse_gelu_matches_composition(oracle, dt):
+    rng = np.random.default_rng(21)
+    x = (rng.standard_normal((9, 2 * 300 + 12)) * 1.5 + 0.3).astype(dt)
+    res = oracle.gelu_and_mul_sparse_typed(x, d=300, z=1.2)
+    want = _torch_composition(torch.from_numpy(x.astype(np.float64)), 300, 1.2).numpy()
+    assert np.allclose(res.ref, want, rtol=1e-12, atol=1e-13)
+    g = x[:, :300].astype(np.float64)
+    assert np.allclose(res.std, g.std(axis=1), rtol=1e-13)
+
+
+def test_typed_sparse_gelu_agrees_with_bf16_path_on_bf16_values(oracle):
+    # bf16 values are exactly representable in fp32: the fp32 path must give
+    # the same result as the bf16 path on the same values
+    inp = W.iid(7, 512, seed=3)
+    a = oracle.gelu_and_mul_sparse(W.to_bits(inp.x), d=512, z=inp.z)
+    b = oracle.gelu_and_mul_sparse_typed(inp.x.float().numpy(), d=512, z=inp.z)
+    assert np.array_equal(a.ref, b.ref) and np.array_equal(a.mask, b.mask)
+
+
+def test_typed_worked_example_fp32(oracle):
+    x = np.array([[1.0, 3.0, 7.0, -2.0]], dtype=np.float32)
+    res = oracle.gelu_and_mul_sparse_typed(x, d=2, z=0.5)
+    g05 = F.gelu(torch.tensor(0.5, dtype=torch.float64), approximate="tanh").item()
+    assert res.ref[0, 0] == 0.0 and res.ref[0, 1] == pytest.approx(-2.0 * g05, rel=1e-15)
