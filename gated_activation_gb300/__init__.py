@@ -20,13 +20,16 @@ LIB_PATH = _build.LIB
 
 OK = 0
 ERR_NULL, ERR_SIZE, ERR_STRIDE, ERR_TOO_LARGE = -1, -2, -3, -4
-ERR_OVERLAP, ERR_VARIANT, ERR_CUDA, ERR_ALIGN = -5, -6, -7, -8
+ERR_OVERLAP, ERR_VARIANT, ERR_CUDA, ERR_ALIGN, ERR_DTYPE = -5, -6, -7, -8, -9
+
+BF16, F16, F32 = 0, 1, 2
+_DTYPE_CODE = {torch.bfloat16: BF16, torch.float16: F16, torch.float32: F32}
 
 VARIANT_AUTO, VARIANT_WARP_ROWS, VARIANT_CTA_ROW, VARIANT_SCALAR, VARIANT_TMA_ROWS = 0, 1, 2, 3, 4
 VARIANT_NAMES = {0: "auto", 1: "warp_rows", 2: "cta_row", 3: "scalar", 4: "tma_rows"}
 
 EXPORTED = (
-    "gelu_and_mul_sparse", "silu_and_mul", "gated_act_status_string",
+    "gelu_and_mul_sparse", "gelu_and_mul_sparse_typed", "silu_and_mul", "gated_act_status_string",
     "gated_act_last_cuda_error", "gelu_and_mul_sparse_plan", "gelu_and_mul_sparse_ex",
     "gated_act_device_status", "gated_act_noop", "silu_and_mul_bounded", "gelu_and_mul",
     "squared_relu",
@@ -76,8 +79,11 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.gelu_and_mul_sparse_ex.argtypes = [vp, cvp, i64, i64, i64, ctypes.c_double,
                                            ctypes.c_int, ctypes.c_int, vp]
     lib.gelu_and_mul_sparse_ex.restype = ctypes.c_int
-    lib.gelu_and_mul_sparse_plan.argtypes = [cvp, cvp, i64, i64, i64, ctypes.c_int,
+    lib.gelu_and_mul_sparse_plan.argtypes = [cvp, cvp, i64, i64, i64, ctypes.c_int, ctypes.c_int,
                                              ctypes.c_int, ctypes.c_int, ctypes.POINTER(Plan)]
+    lib.gelu_and_mul_sparse_typed.argtypes = [vp, cvp, i64, i64, i64, ctypes.c_double,
+                                              ctypes.c_int, ctypes.c_int, ctypes.c_int, vp]
+    lib.gelu_and_mul_sparse_typed.restype = ctypes.c_int
     lib.gelu_and_mul_sparse_plan.restype = ctypes.c_int
     lib.silu_and_mul.argtypes = [vp, cvp, i64, i64, vp]
     lib.silu_and_mul.restype = ctypes.c_int
@@ -117,12 +123,12 @@ def _stream_handle(stream: torch.cuda.Stream | None) -> int:
     return int(s.cuda_stream)
 
 
-def _rows_view(x: torch.Tensor) -> tuple[int, int]:
-    """(T, row_stride) for a 2-D bf16 CUDA tensor whose rows may be strided."""
+def _rows_view(x: torch.Tensor, dtypes=(torch.bfloat16,)) -> tuple[int, int]:
+    """(T, row_stride) for a 2-D CUDA tensor whose rows may be strided."""
     if x.dim() != 2:
         raise ValueError("input must be 2-D [T, row_stride]")
-    if x.dtype != torch.bfloat16:
-        raise TypeError("input must be bfloat16")
+    if x.dtype not in dtypes:
+        raise TypeError(f"input must be one of {dtypes}")
     if not x.is_cuda:
         raise ValueError("input must be a CUDA tensor (the library has no CPU path)")
     if x.stride(1) != 1:
@@ -133,12 +139,13 @@ def _rows_view(x: torch.Tensor) -> tuple[int, int]:
 def gelu_and_mul_sparse(x: torch.Tensor, z: float, d: int | None = None,
                         out: torch.Tensor | None = None, variant: int = VARIANT_AUTO,
                         cluster: int = 0, stream: torch.cuda.Stream | None = None) -> torch.Tensor:
-    """Sparse GELU gate of ``x`` ([T, >=2d] bf16 CUDA): returns ``out`` [T, d] bf16.
+    """Sparse GELU gate of ``x`` ([T, >=2d] bf16, fp16 or fp32 CUDA): returns
+    ``out`` [T, d] of the same type.
 
     ``d`` defaults to half the row length.  Rows may be strided (x[:, :2d] of a
     wider buffer).  ``variant``/``cluster`` force a launch geometry.
     """
-    T, rs = _rows_view(x)
+    T, rs = _rows_view(x, tuple(_DTYPE_CODE))
     if d is None:
         if x.shape[1] % 2:
             raise ValueError("odd row length: pass d explicitly")
@@ -146,12 +153,13 @@ def gelu_and_mul_sparse(x: torch.Tensor, z: float, d: int | None = None,
     if x.shape[1] < 2 * d:
         raise ValueError("rows are shorter than 2d")
     if out is None:
-        out = torch.empty((T, d), dtype=torch.bfloat16, device=x.device)
-    elif out.shape != (T, d) or out.dtype != torch.bfloat16 or not out.is_contiguous():
-        raise ValueError("out must be a contiguous [T, d] bf16 tensor")
+        out = torch.empty((T, d), dtype=x.dtype, device=x.device)
+    elif out.shape != (T, d) or out.dtype != x.dtype or not out.is_contiguous():
+        raise ValueError(f"out must be a contiguous [T, d] {x.dtype} tensor")
     lib = load_library()
-    rc = lib.gelu_and_mul_sparse_ex(out.data_ptr(), x.data_ptr(), T, d, rs, float(z),
-                                    int(variant), int(cluster), _stream_handle(stream))
+    rc = lib.gelu_and_mul_sparse_typed(out.data_ptr(), x.data_ptr(), T, d, rs, float(z),
+                                       _DTYPE_CODE[x.dtype], int(variant), int(cluster),
+                                       _stream_handle(stream))
     _check("gelu_and_mul_sparse", rc)
     return out
 
@@ -159,12 +167,13 @@ def gelu_and_mul_sparse(x: torch.Tensor, z: float, d: int | None = None,
 def gelu_and_mul_sparse_plan(x: torch.Tensor, d: int | None = None, out: torch.Tensor | None = None,
                              variant: int = VARIANT_AUTO, cluster: int = 0) -> dict:
     """The launch geometry gelu_and_mul_sparse would use for this call."""
-    T, rs = _rows_view(x)
+    T, rs = _rows_view(x, tuple(_DTYPE_CODE))
     d = int(x.shape[1]) // 2 if d is None else d
     p = Plan()
     out_ptr = out.data_ptr() if out is not None else 0
     rc = load_library().gelu_and_mul_sparse_plan(out_ptr, x.data_ptr(), T, d, rs,
-                                                 int(variant), int(cluster), 0, ctypes.byref(p))
+                                                 _DTYPE_CODE[x.dtype], int(variant), int(cluster),
+                                                 0, ctypes.byref(p))
     _check("gelu_and_mul_sparse_plan", rc)
     return p.as_dict()
 

@@ -5,6 +5,7 @@
 
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 #include "gated_act.h"
@@ -29,6 +30,12 @@ __device__ __forceinline__ uint4 ld_stream(const void *p) {
     asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
         : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
         : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t ld_stream_u32(const uint32_t *p) {
+    uint32_t r;
+    asm("ld.global.nc.u32 %0, [%1];" : "=r"(r) : "l"(p));
     return r;
 }
 

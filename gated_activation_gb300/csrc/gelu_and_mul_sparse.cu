@@ -103,41 +103,103 @@ __device__ __forceinline__ float tanh_approx(float x) {
     return y;
 }
 
-// Two outputs gelu_tanh(max(g - cutoff, 0)) * u from one gate word and one up word.
-__device__ __forceinline__ uint32_t epi2(uint32_t gw, uint32_t uw, float2 c2) {
-    float2 s = sub2(unpack2(gw), c2);
-    s.x = relu_nan(s.x);
-    s.y = relu_nan(s.y);
-    const float2 y = mul2(s, fma2(mul2(s, s), make_float2(kCubicCoef, kCubicCoef),
-                                  make_float2(kSqrt2OverPi, kSqrt2OverPi)));
-    const float2 h = mul2(s, make_float2(0.5f, 0.5f));
-    const float2 a = fma2(h, make_float2(tanh_approx(y.x), tanh_approx(y.y)), h);
-    const float2 o = mul2(a, unpack2(uw));
-    return pack_bf16x2(o.x, o.y);
-}
+// ------------------------------------------------------------ element formats
+// A 16-byte vector holds kPairs pairs of elements: pair(v, i) reads pair i as
+// fp32, put_pair writes pair i rounded to the format (nearest even).  tanh is
+// the hardware approximation for the 16-bit formats (its 2^-12 relative error
+// in 1 + tanh is below their rounding) and the accurate libm-style tanhf for
+// fp32 outputs.
+struct FmtBf16 {
+    static constexpr int kElem = 2, kPairs = 4;
+    __device__ static float2 pair(const uint4 &v, int i) { return unpack2((&v.x)[i]); }
+    __device__ static void put_pair(uint4 &v, int i, float2 f) {
+        (&v.x)[i] = pack_bf16x2(f.x, f.y);
+    }
+    __device__ static float tanh(float x) { return tanh_approx(x); }
+    __device__ static float load1(const uint8_t *p) {
+        return __uint_as_float(static_cast<uint32_t>(ld_stream_u16(reinterpret_cast<const uint16_t *>(p))) << 16);
+    }
+    __device__ static void store1(uint8_t *p, float f) {
+        *reinterpret_cast<uint16_t *>(p) = __bfloat16_as_ushort(__float2bfloat16_rn(f));
+    }
+};
 
-__device__ __forceinline__ uint4 epilogue8(uint4 g, uint4 u, float cutoff) {
+struct FmtF16 {
+    static constexpr int kElem = 2, kPairs = 4;
+    __device__ static float2 pair(const uint4 &v, int i) {
+        const uint32_t w = (&v.x)[i];
+        return __half22float2(*reinterpret_cast<const __half2 *>(&w));
+    }
+    __device__ static void put_pair(uint4 &v, int i, float2 f) {
+        const __half2 h = __floats2half2_rn(f.x, f.y);
+        (&v.x)[i] = *reinterpret_cast<const uint32_t *>(&h);
+    }
+    __device__ static float tanh(float x) { return tanh_approx(x); }
+    __device__ static float load1(const uint8_t *p) {
+        return __half2float(__ushort_as_half(ld_stream_u16(reinterpret_cast<const uint16_t *>(p))));
+    }
+    __device__ static void store1(uint8_t *p, float f) {
+        *reinterpret_cast<uint16_t *>(p) = __half_as_ushort(__float2half_rn(f));
+    }
+};
+
+struct FmtF32 {
+    static constexpr int kElem = 4, kPairs = 2;
+    __device__ static float2 pair(const uint4 &v, int i) {
+        return i == 0 ? make_float2(__uint_as_float(v.x), __uint_as_float(v.y))
+                      : make_float2(__uint_as_float(v.z), __uint_as_float(v.w));
+    }
+    __device__ static void put_pair(uint4 &v, int i, float2 f) {
+        if (i == 0) {
+            v.x = __float_as_uint(f.x);
+            v.y = __float_as_uint(f.y);
+        } else {
+            v.z = __float_as_uint(f.x);
+            v.w = __float_as_uint(f.y);
+        }
+    }
+    __device__ static float tanh(float x) { return tanhf(x); }
+    __device__ static float load1(const uint8_t *p) {
+        return __uint_as_float(ld_stream_u32(reinterpret_cast<const uint32_t *>(p)));
+    }
+    __device__ static void store1(uint8_t *p, float f) { *reinterpret_cast<float *>(p) = f; }
+};
+
+// gelu_tanh(max(g - cutoff, 0)) * u for every element of one 16-byte vector.
+template <class F>
+__device__ __forceinline__ uint4 epi_vec(const uint4 &g, const uint4 &u, float cutoff) {
     const float2 c2 = make_float2(cutoff, cutoff);
-    return make_uint4(epi2(g.x, u.x, c2), epi2(g.y, u.y, c2), epi2(g.z, u.z, c2),
-                      epi2(g.w, u.w, c2));
+    uint4 o;
+#pragma unroll
+    for (int i = 0; i < F::kPairs; ++i) {
+        float2 s = sub2(F::pair(g, i), c2);
+        s.x = relu_nan(s.x);
+        s.y = relu_nan(s.y);
+        const float2 y = mul2(s, fma2(mul2(s, s), make_float2(kCubicCoef, kCubicCoef),
+                                      make_float2(kSqrt2OverPi, kSqrt2OverPi)));
+        const float2 h = mul2(s, make_float2(0.5f, 0.5f));
+        const float2 a = fma2(h, make_float2(F::tanh(y.x), F::tanh(y.y)), h);
+        F::put_pair(o, i, mul2(a, F::pair(u, i)));
+    }
+    return o;
 }
 
-// Running pair sums over 8 gate values.
-__device__ __forceinline__ float2 sum8(float2 acc, uint4 g) {
-    acc = add2(acc, unpack2(g.x));
-    acc = add2(acc, unpack2(g.y));
-    acc = add2(acc, unpack2(g.z));
-    return add2(acc, unpack2(g.w));
+// Running pair sums over one vector of gate values.
+template <class F>
+__device__ __forceinline__ float2 sum_vec(float2 acc, const uint4 &g) {
+#pragma unroll
+    for (int i = 0; i < F::kPairs; ++i)
+        acc = add2(acc, F::pair(g, i));
+    return acc;
 }
-__device__ __forceinline__ float2 ssd8(float2 acc, uint4 g, float2 m2) {
-    float2 e = sub2(unpack2(g.x), m2);
-    acc = fma2(e, e, acc);
-    e = sub2(unpack2(g.y), m2);
-    acc = fma2(e, e, acc);
-    e = sub2(unpack2(g.z), m2);
-    acc = fma2(e, e, acc);
-    e = sub2(unpack2(g.w), m2);
-    return fma2(e, e, acc);
+template <class F>
+__device__ __forceinline__ float2 ssd_vec(float2 acc, const uint4 &g, float2 m2) {
+#pragma unroll
+    for (int i = 0; i < F::kPairs; ++i) {
+        const float2 e = sub2(F::pair(g, i), m2);
+        acc = fma2(e, e, acc);
+    }
+    return acc;
 }
 
 // CTA-wide sum; every thread returns the same bits.
@@ -288,7 +350,7 @@ gelu_tma_rows(uint16_t *__restrict__ out, const uint16_t *__restrict__ in, int64
         float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
         for (int i = 0; i < V; ++i)
-            acc = sum8(acc, g[i]);
+            acc = sum_vec<FmtBf16>(acc, g[i]);
         float s = warp_sum(acc.x + acc.y);
         if (lane == 0)
             red[0][warp] = s;
@@ -303,7 +365,7 @@ gelu_tma_rows(uint16_t *__restrict__ out, const uint16_t *__restrict__ in, int64
 #pragma unroll
         for (int i = 0; i < V; ++i)
             if (tid + NT * i < nvec)
-                acc = ssd8(acc, g[i], m2);
+                acc = ssd_vec<FmtBf16>(acc, g[i], m2);
         const float q = block_sum<NW>(acc.x + acc.y, red[1], lane, warp);
         const float sd = __fsqrt_rn(__fdiv_rn(q, static_cast<float>(d)));
         const float cutoff = fmaf(sd, z, mean);
@@ -316,7 +378,7 @@ gelu_tma_rows(uint16_t *__restrict__ out, const uint16_t *__restrict__ in, int64
             for (int i = 0; i < V; ++i) {
                 const int v = tid + NT * i;
                 if (v < nvec)
-                    st_vec(op + 8 * v, epilogue8(g[i], us[v], cutoff));
+                    st_vec(op + 8 * v, epi_vec<FmtBf16>(g[i], us[v], cutoff));
             }
         }
     }
@@ -364,14 +426,14 @@ gelu_warp_rows(uint16_t *__restrict__ out, const uint16_t *__restrict__ in, int6
     float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
     for (int i = 0; i < V; ++i)
-        acc = sum8(acc, g[i]);
+        acc = sum_vec<FmtBf16>(acc, g[i]);
     const float mean = __fdiv_rn(warp_sum(acc.x + acc.y), static_cast<float>(d));
     const float2 m2 = make_float2(mean, mean);
     acc = make_float2(0.f, 0.f);
 #pragma unroll
     for (int i = 0; i < V; ++i)
         if (lane + 32 * i < nvec)
-            acc = ssd8(acc, g[i], m2);
+            acc = ssd_vec<FmtBf16>(acc, g[i], m2);
     const float q = warp_sum(acc.x + acc.y);
     const float sd = __fsqrt_rn(__fdiv_rn(q, static_cast<float>(d)));
     const float cutoff = fmaf(sd, z, mean);
@@ -381,54 +443,59 @@ gelu_warp_rows(uint16_t *__restrict__ out, const uint16_t *__restrict__ in, int6
     for (int i = 0; i < V; ++i) {
         const int v = lane + 32 * i;
         if (v < nvec)
-            st_vec(op + 8 * v, epilogue8(g[i], u[i], cutoff));
+            st_vec(op + 8 * v, epi_vec<FmtBf16>(g[i], u[i], cutoff));
     }
 }
 
 // ------------------------------------------------------------ CTA / cluster rows
 // A cluster of C CTAs (C = 1: a lone CTA) owns one row at a time; CTA k of
-// the cluster holds gate/up vectors [k sv, min((k+1) sv, d/8)), thread t the
-// vectors k sv + t + NT i.  Rows advance by the number of clusters in the grid.
-// CL = false: C must be 1 (no cluster code is compiled in).
-template <int NT, int V, bool CL>
+// the cluster holds gate/up vectors [k sv, min((k+1) sv, nvec)) of 16 bytes,
+// thread t the vectors k sv + t + NT i.  Rows advance by the number of
+// clusters in the grid.  CL = false: C must be 1 (no cluster code is
+// compiled in).  F is the element format.
+template <int NT, int V, bool CL, class F>
 __global__ void __launch_bounds__(NT, (1024 / NT) > 0 ? (1024 / NT) : 1)
-gelu_cta_rows(uint16_t *__restrict__ out, const uint16_t *__restrict__ in, int64_t T, int d,
+gelu_cta_rows(void *__restrict__ out_, const void *__restrict__ in_, int64_t T, int d,
               int64_t rs, float z, int C, int sv) {
     constexpr int NW = NT / 32;
+    constexpr int kEpv = 16 / F::kElem;   // elements per 16-byte vector
     __shared__ float red[2][NW];
     __shared__ float xch[3];   // this CTA's (element count, sum, M2) for its peers
 
     if (!CL)
         C = 1;
+    const uint8_t *in = static_cast<const uint8_t *>(in_);
+    uint8_t *out = static_cast<uint8_t *>(out_);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int rank = CL ? static_cast<int>(cluster_ctarank()) : 0;
-    const int nvec = d >> 3;
+    const int nvec = d / kEpv;
     const int v0 = rank * sv;
     const int v1 = min(nvec, v0 + sv);
-    const int nk = max(v1 - v0, 0) * 8;
+    const int nk = max(v1 - v0, 0) * kEpv;
     const int64_t nclusters = gridDim.x / C;
+    const int64_t rs_bytes = rs * F::kElem, d_bytes = static_cast<int64_t>(d) * F::kElem;
     pdl_wait();
     pdl_trigger();
 
     for (int64_t row = blockIdx.x / C; row < T; row += nclusters) {
-        const uint16_t *gp = in + row * rs;
-        const uint16_t *up = gp + d;
+        const uint8_t *gp = in + row * rs_bytes;
+        const uint8_t *up = gp + d_bytes;
         uint4 g[V], u[V];
 #pragma unroll
         for (int i = 0; i < V; ++i) {
             const int v = v0 + tid + NT * i;
             if (v < v1) {
-                g[i] = ld_stream(gp + 8 * v);
-                u[i] = ld_stream(up + 8 * v);
+                g[i] = ld_stream(gp + 16 * v);
+                u[i] = ld_stream(up + 16 * v);
             } else {
-                g[i] = make_uint4(0u, 0u, 0u, 0u);
+                g[i] = make_uint4(0u, 0u, 0u, 0u);   // +0 in every format
                 u[i] = g[i];
             }
         }
         float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
         for (int i = 0; i < V; ++i)
-            acc = sum8(acc, g[i]);
+            acc = sum_vec<F>(acc, g[i]);
         const float s = block_sum<NW>(acc.x + acc.y, red[0], lane, warp);
 
         float mean, var;
@@ -439,7 +506,7 @@ gelu_cta_rows(uint16_t *__restrict__ out, const uint16_t *__restrict__ in, int64
 #pragma unroll
             for (int i = 0; i < V; ++i)
                 if (v0 + tid + NT * i < v1)
-                    acc = ssd8(acc, g[i], m2);
+                    acc = ssd_vec<F>(acc, g[i], m2);
             var = __fdiv_rn(block_sum<NW>(acc.x + acc.y, red[1], lane, warp),
                             static_cast<float>(d));
         } else {
@@ -450,7 +517,7 @@ gelu_cta_rows(uint16_t *__restrict__ out, const uint16_t *__restrict__ in, int64
 #pragma unroll
             for (int i = 0; i < V; ++i)
                 if (v0 + tid + NT * i < v1)
-                    acc = ssd8(acc, g[i], m2);
+                    acc = ssd_vec<F>(acc, g[i], m2);
             const float q = block_sum<NW>(acc.x + acc.y, red[1], lane, warp);
             if (tid == 0) {
                 xch[0] = static_cast<float>(nk);
@@ -479,12 +546,12 @@ gelu_cta_rows(uint16_t *__restrict__ out, const uint16_t *__restrict__ in, int64
         const float sd = __fsqrt_rn(var);
         const float cutoff = fmaf(sd, z, mean);
 
-        uint16_t *op = out + row * static_cast<int64_t>(d);
+        uint8_t *op = out + row * d_bytes;
 #pragma unroll
         for (int i = 0; i < V; ++i) {
             const int v = v0 + tid + NT * i;
             if (v < v1)
-                st_vec(op + 8 * v, epilogue8(g[i], u[i], cutoff));
+                st_vec(op + 16 * v, epi_vec<F>(g[i], u[i], cutoff));
         }
         if (CL)
             cluster_wait_acquire();   // peers are done with xch before it changes
@@ -492,54 +559,54 @@ gelu_cta_rows(uint16_t *__restrict__ out, const uint16_t *__restrict__ in, int64
 }
 
 // ------------------------------------------------------------ scalar rows
-// Any layout: one CTA per row, 2-byte loads; each pass re-reads the gate
-// (from L1/L2 after the first pass).
-__device__ __forceinline__ float ld_bf16(const uint16_t *p) {
-    return __uint_as_float(static_cast<uint32_t>(ld_stream_u16(p)) << 16);
-}
-
-__device__ __forceinline__ float sparse_gelu_mul(float g, float u, float cutoff) {
+// Any layout: one CTA per row, one element per access; each pass re-reads
+// the gate (from L1/L2 after the first pass).
+__device__ __forceinline__ float sparse_gelu_mul(float g, float u, float cutoff, bool exact_tanh) {
     const float s = relu_nan(g - cutoff);
     const float y = s * fmaf(kCubicCoef, s * s, kSqrt2OverPi);
     const float h = 0.5f * s;
-    return fmaf(h, tanh_approx(y), h) * u;
+    return fmaf(h, exact_tanh ? tanhf(y) : tanh_approx(y), h) * u;
 }
 
+template <class F>
 __global__ void __launch_bounds__(kScalarThreads)
-gelu_scalar_rows(uint16_t *__restrict__ out, const uint16_t *__restrict__ in, int64_t T,
-                 int64_t d, int64_t rs, float z) {
+gelu_scalar_rows(void *__restrict__ out_, const void *__restrict__ in_, int64_t T, int64_t d,
+                 int64_t rs, float z) {
     constexpr int NW = kScalarThreads / 32;
+    constexpr int64_t E = F::kElem;
     __shared__ float red[2][NW];
+    const uint8_t *in = static_cast<const uint8_t *>(in_);
+    uint8_t *out = static_cast<uint8_t *>(out_);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     pdl_wait();
     pdl_trigger();
     for (int64_t row = blockIdx.x; row < T; row += gridDim.x) {
-        const uint16_t *gp = in + row * rs;
-        const uint16_t *up = gp + d;
+        const uint8_t *gp = in + row * rs * E;
+        const uint8_t *up = gp + d * E;
         float s = 0.f;
         for (int64_t j = tid; j < d; j += kScalarThreads)
-            s += ld_bf16(gp + j);
+            s += F::load1(gp + j * E);
         s = block_sum<NW>(s, red[0], lane, warp);
         const float mean = __fdiv_rn(s, static_cast<float>(d));
         float q = 0.f;
         for (int64_t j = tid; j < d; j += kScalarThreads) {
-            const float e = ld_bf16(gp + j) - mean;
+            const float e = F::load1(gp + j * E) - mean;
             q = fmaf(e, e, q);
         }
         q = block_sum<NW>(q, red[1], lane, warp);
         const float sd = __fsqrt_rn(__fdiv_rn(q, static_cast<float>(d)));
         const float cutoff = fmaf(sd, z, mean);
-        uint16_t *op = out + row * d;
-        for (int64_t j = tid; j < d; j += kScalarThreads) {
-            const float y = sparse_gelu_mul(ld_bf16(gp + j), ld_bf16(up + j), cutoff);
-            op[j] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
-        }
+        uint8_t *op = out + row * d * E;
+        for (int64_t j = tid; j < d; j += kScalarThreads)
+            F::store1(op + j * E, sparse_gelu_mul(F::load1(gp + j * E), F::load1(up + j * E),
+                                                  cutoff, E == 4));
     }
 }
 
 // ------------------------------------------------------------ host side
 using WarpFn = void (*)(uint16_t *, const uint16_t *, int64_t, int, int64_t, float);
-using CtaFn = void (*)(uint16_t *, const uint16_t *, int64_t, int, int64_t, float, int, int);
+using CtaFn = void (*)(void *, const void *, int64_t, int, int64_t, float, int, int);
+using ScalarFn = void (*)(void *, const void *, int64_t, int64_t, int64_t, float);
 using TmaFn = void (*)(uint16_t *, const uint16_t *, int64_t, int, int64_t, float, int);
 
 WarpFn warp_fn(int v) {
@@ -552,31 +619,50 @@ WarpFn warp_fn(int v) {
     }
 }
 
-template <bool CL>
+template <bool CL, class F>
 CtaFn cta_fn_t(int nt, int v) {
     if (v == 2) {
         switch (nt) {
-        case 64: return gelu_cta_rows<64, 2, CL>;
-        case 128: return gelu_cta_rows<128, 2, CL>;
+        case 64: return gelu_cta_rows<64, 2, CL, F>;
+        case 128: return gelu_cta_rows<128, 2, CL, F>;
         default: return nullptr;
         }
     }
     if (v == 4) {
         switch (nt) {
-        case 64: return gelu_cta_rows<64, 4, CL>;
-        case 128: return gelu_cta_rows<128, 4, CL>;
-        case 256: return gelu_cta_rows<256, 4, CL>;
-        case 512: return gelu_cta_rows<512, 4, CL>;
-        case 1024: return gelu_cta_rows<1024, 4, CL>;
+        case 64: return gelu_cta_rows<64, 4, CL, F>;
+        case 128: return gelu_cta_rows<128, 4, CL, F>;
+        case 256: return gelu_cta_rows<256, 4, CL, F>;
+        case 512: return gelu_cta_rows<512, 4, CL, F>;
+        case 1024: return gelu_cta_rows<1024, 4, CL, F>;
         default: return nullptr;
         }
     }
     return nullptr;
 }
 
-CtaFn cta_fn(int nt, int v, int cluster) {
-    return cluster > 1 ? cta_fn_t<true>(nt, v) : cta_fn_t<false>(nt, v);
+template <class F>
+CtaFn cta_fn_f(int nt, int v, int cluster) {
+    return cluster > 1 ? cta_fn_t<true, F>(nt, v) : cta_fn_t<false, F>(nt, v);
 }
+
+CtaFn cta_fn(int nt, int v, int cluster, int dtype) {
+    switch (dtype) {
+    case GATED_ACT_F16: return cta_fn_f<FmtF16>(nt, v, cluster);
+    case GATED_ACT_F32: return cta_fn_f<FmtF32>(nt, v, cluster);
+    default: return cta_fn_f<FmtBf16>(nt, v, cluster);
+    }
+}
+
+ScalarFn scalar_fn(int dtype) {
+    switch (dtype) {
+    case GATED_ACT_F16: return gelu_scalar_rows<FmtF16>;
+    case GATED_ACT_F32: return gelu_scalar_rows<FmtF32>;
+    default: return gelu_scalar_rows<FmtBf16>;
+    }
+}
+
+int elem_bytes(int dtype) { return dtype == GATED_ACT_F32 ? 4 : 2; }
 
 TmaFn tma_fn(int nt) {
     switch (nt) {
@@ -601,7 +687,8 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 struct Plan {
     gated_act_plan pub;
-    int sv;   // vectors per CTA slice (CTA rows)
+    int sv;      // vectors per CTA slice (CTA rows)
+    int dtype;   // gated_act_dtype of in and out
 };
 
 // Threads and vectors per thread for a CTA slice of sv vectors.
@@ -658,7 +745,7 @@ bool tma_shape(int64_t nvec, int want_cps, int *cps, int *nt, int *stages, int64
 }
 
 // check_ptrs = false (plan queries): pointers are only inspected for alignment.
-int validate(const void *out, const void *in, int64_t T, int64_t d, int64_t rs,
+int validate(const void *out, const void *in, int64_t T, int64_t d, int64_t rs, int elem,
              bool check_ptrs) {
     if (T < 0 || d <= 0)
         return GATED_ACT_ERR_SIZE;
@@ -670,32 +757,41 @@ int validate(const void *out, const void *in, int64_t T, int64_t d, int64_t rs,
         return GATED_ACT_OK;
     if (!out || !in)
         return GATED_ACT_ERR_NULL;
-    if (!aligned(out, 2) || !aligned(in, 2))
+    if (!aligned(out, elem) || !aligned(in, elem))
         return GATED_ACT_ERR_ALIGN;
-    const uint64_t in_bytes = 2ull * static_cast<uint64_t>((T - 1) * rs + 2 * d);
-    const uint64_t out_bytes = 2ull * static_cast<uint64_t>(T * d);
+    const uint64_t in_bytes = elem * static_cast<uint64_t>((T - 1) * rs + 2 * d);
+    const uint64_t out_bytes = elem * static_cast<uint64_t>(T * d);
     if (ranges_overlap(out, out_bytes, in, in_bytes))
         return GATED_ACT_ERR_OVERLAP;
     return GATED_ACT_OK;
 }
 
-int make_plan(const void *out, const void *in, int64_t T, int64_t d, int64_t rs,
+int make_plan(const void *out, const void *in, int64_t T, int64_t d, int64_t rs, int dtype,
               int variant, int cluster, int sm_count, bool check_ptrs, Plan *p) {
-    const int rc = validate(out, in, T, d, rs, check_ptrs);
+    if (dtype < GATED_ACT_BF16 || dtype > GATED_ACT_F32)
+        return GATED_ACT_ERR_DTYPE;
+    const int elem = elem_bytes(dtype), epv = 16 / elem;
+    const int rc = validate(out, in, T, d, rs, elem, check_ptrs);
     if (rc != GATED_ACT_OK)
         return rc;
     if (variant < GATED_ACT_VARIANT_AUTO || variant > GATED_ACT_VARIANT_TMA_ROWS)
         return GATED_ACT_ERR_VARIANT;
+    // the warp-rows and TMA-rows kernels exist for bf16 only
+    if (dtype != GATED_ACT_BF16 &&
+        (variant == GATED_ACT_VARIANT_WARP_ROWS || variant == GATED_ACT_VARIANT_TMA_ROWS))
+        return GATED_ACT_ERR_VARIANT;
     gated_act_plan &q = p->pub;
     q = gated_act_plan{};
     p->sv = 0;
-    const bool vec_ok = aligned(in, 16) && aligned(out, 16) && d % 8 == 0 && rs % 8 == 0;
-    const int64_t nvec = d / 8;
+    p->dtype = dtype;
+    const bool vec_ok = aligned(in, 16) && aligned(out, 16) && d % epv == 0 && rs % epv == 0;
+    const int64_t nvec = d / epv;
     const int sms = sm_count > 0 ? sm_count : (T > 0 ? device_sm_count() : 1);
     int t_cps = 0, t_nt = 0, t_stages = 0;
     int64_t t_smem = 0;
     const int want_cps = variant == GATED_ACT_VARIANT_TMA_ROWS ? cluster : 0;
-    const bool tma_ok = vec_ok && tma_shape(nvec, want_cps, &t_cps, &t_nt, &t_stages, &t_smem);
+    const bool tma_ok = vec_ok && dtype == GATED_ACT_BF16 &&
+                        tma_shape(nvec, want_cps, &t_cps, &t_nt, &t_stages, &t_smem);
 
     // Measured on GB300 (every geometry timed per T x d, graph-replayed over
     // rotating buffers): persistent TMA rows win only for the widest rows at
@@ -707,7 +803,7 @@ int make_plan(const void *out, const void *in, int64_t T, int64_t d, int64_t rs,
             variant = GATED_ACT_VARIANT_SCALAR;
         else if (tma_ok && ((nvec >= 4096 && T >= 3 * sm) || (nvec >= 2048 && T >= 12 * sm)))
             variant = GATED_ACT_VARIANT_TMA_ROWS;
-        else if (nvec <= 64)
+        else if (nvec <= 64 && dtype == GATED_ACT_BF16)
             variant = GATED_ACT_VARIANT_WARP_ROWS;
         else
             variant = GATED_ACT_VARIANT_CTA_ROW;
@@ -833,15 +929,15 @@ int launch(const Plan &p, void *out, const void *in, int64_t T, int64_t d, int64
         e = launch_kernel(warp_fn(q.vec_per_thread), grid, block, 0, stream, 1, o, x, T, di, rs, zf);
         break;
     case GATED_ACT_VARIANT_CTA_ROW: {
-        CtaFn fn = cta_fn(q.threads, q.vec_per_thread, q.cluster);
+        CtaFn fn = cta_fn(q.threads, q.vec_per_thread, q.cluster, p.dtype);
         if (!fn)
             return GATED_ACT_ERR_VARIANT;
-        e = launch_kernel(fn, grid, block, 0, stream, q.cluster, o, x, T, di, rs, zf,
+        e = launch_kernel(fn, grid, block, 0, stream, q.cluster, out, in, T, di, rs, zf,
                           static_cast<int>(q.cluster), p.sv);
         break;
     }
     default:
-        e = launch_kernel(gelu_scalar_rows, grid, block, 0, stream, 1, o, x, T, d, rs, zf);
+        e = launch_kernel(scalar_fn(p.dtype), grid, block, 0, stream, 1, out, in, T, d, rs, zf);
         break;
     }
     if (e != cudaSuccess)
@@ -853,32 +949,41 @@ int launch(const Plan &p, void *out, const void *in, int64_t T, int64_t d, int64
 }  // namespace gact
 
 extern "C" int gelu_and_mul_sparse_plan(const void *out, const void *in, int64_t T, int64_t d,
-                                        int64_t row_stride, int variant, int cluster,
+                                        int64_t row_stride, int dtype, int variant, int cluster,
                                         int sm_count, gated_act_plan *plan) {
     if (!plan)
         return GATED_ACT_ERR_NULL;
     gact::Plan p;
-    const int rc = gact::make_plan(out, in, T, d, row_stride, variant, cluster, sm_count, false, &p);
+    const int rc = gact::make_plan(out, in, T, d, row_stride, dtype, variant, cluster, sm_count,
+                                   false, &p);
     if (rc != GATED_ACT_OK)
         return rc;
     *plan = p.pub;
     return GATED_ACT_OK;
 }
 
-extern "C" int gelu_and_mul_sparse_ex(void *out, const void *in, int64_t T, int64_t d,
-                                      int64_t row_stride, double z, int variant, int cluster,
-                                      cudaStream_t stream) {
+extern "C" int gelu_and_mul_sparse_typed(void *out, const void *in, int64_t T, int64_t d,
+                                         int64_t row_stride, double z, int dtype, int variant,
+                                         int cluster, cudaStream_t stream) {
     gact::Plan p;
-    const int rc = gact::make_plan(out, in, T, d, row_stride, variant, cluster, 0, true, &p);
+    const int rc =
+        gact::make_plan(out, in, T, d, row_stride, dtype, variant, cluster, 0, true, &p);
     if (rc != GATED_ACT_OK || T == 0)
         return rc;
     return gact::launch(p, out, in, T, d, row_stride, z, stream);
 }
 
+extern "C" int gelu_and_mul_sparse_ex(void *out, const void *in, int64_t T, int64_t d,
+                                      int64_t row_stride, double z, int variant, int cluster,
+                                      cudaStream_t stream) {
+    return gelu_and_mul_sparse_typed(out, in, T, d, row_stride, z, GATED_ACT_BF16, variant,
+                                     cluster, stream);
+}
+
 extern "C" int gelu_and_mul_sparse(void *out, const void *in, int64_t T, int64_t d,
                                    int64_t row_stride, double z, cudaStream_t stream) {
-    return gelu_and_mul_sparse_ex(out, in, T, d, row_stride, z, GATED_ACT_VARIANT_AUTO, 0,
-                                  stream);
+    return gelu_and_mul_sparse_typed(out, in, T, d, row_stride, z, GATED_ACT_BF16,
+                                     GATED_ACT_VARIANT_AUTO, 0, stream);
 }
 
 extern "C" int gated_act_device_status(unsigned int *flags) {

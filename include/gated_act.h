@@ -60,8 +60,16 @@ typedef enum gated_act_status {
     GATED_ACT_ERR_OVERLAP = -5,    /* the bytes out writes overlap the bytes in reads */
     GATED_ACT_ERR_VARIANT = -6,    /* a forced variant/cluster size does not fit the call */
     GATED_ACT_ERR_CUDA = -7,       /* the CUDA runtime reported an error at launch */
-    GATED_ACT_ERR_ALIGN = -8       /* a pointer is not 2-byte aligned            */
+    GATED_ACT_ERR_ALIGN = -8,      /* a pointer is not aligned to its element size */
+    GATED_ACT_ERR_DTYPE = -9       /* unknown element type                        */
 } gated_act_status;
+
+/* Element types of the typed entry point (in and out share one type). */
+typedef enum gated_act_dtype {
+    GATED_ACT_BF16 = 0,
+    GATED_ACT_F16 = 1,
+    GATED_ACT_F32 = 2
+} gated_act_dtype;
 
 /*
  * gelu_and_mul_sparse -- fused sparse GELU gate (definition above).
@@ -190,16 +198,18 @@ typedef struct gated_act_plan {
 } gated_act_plan;
 
 /*
- * Describe the launch gelu_and_mul_sparse(_ex) would make, without launching.
- * variant/cluster as in gelu_and_mul_sparse_ex; out/in are only inspected for
+ * Describe the launch gelu_and_mul_sparse(_ex, _typed) would make, without
+ * launching.  dtype a gated_act_dtype; variant/cluster as in
+ * gelu_and_mul_sparse_ex; out/in are only inspected for
  * alignment (never dereferenced).  sm_count > 0 plans for a device with that
  * many SMs; sm_count <= 0 queries the current device (its only CUDA call).
  * Returns 0 and fills *plan, or a negative status (GATED_ACT_ERR_VARIANT when
  * the forced geometry does not fit).
  */
 int gelu_and_mul_sparse_plan(const void *out, const void *in, int64_t T,
-                             int64_t d, int64_t row_stride, int variant,
-                             int cluster, int sm_count, gated_act_plan *plan);
+                             int64_t d, int64_t row_stride, int dtype,
+                             int variant, int cluster, int sm_count,
+                             gated_act_plan *plan);
 
 /*
  * gelu_and_mul_sparse with a forced geometry.
@@ -219,6 +229,24 @@ int gelu_and_mul_sparse_plan(const void *out, const void *in, int64_t T,
 int gelu_and_mul_sparse_ex(void *out, const void *in, int64_t T, int64_t d,
                            int64_t row_stride, double z, int variant,
                            int cluster, cudaStream_t stream);
+
+/*
+ * gelu_and_mul_sparse on fp16 or fp32 rows as well as bf16.  The
+ * sparse-GELU page, "Cross-architecture warp and dtype validation", checks
+ * the op in FP32, FP16 and BF16.
+ *   dtype    a gated_act_dtype shared by in and out.  Sizes and strides are
+ *            in elements; pointers aligned to the element size.
+ *   variant, cluster as in gelu_and_mul_sparse_ex.  fp16 and fp32 run the
+ *            CTA-row (or scalar) geometry only: WARP_ROWS and TMA_ROWS
+ *            return GATED_ACT_ERR_VARIANT for them.
+ * Math is fp32 throughout; the fp32 output uses an accurate tanh, the 16-bit
+ * outputs the hardware approximation.  Accuracy against an fp64 evaluation:
+ * bf16 1e-2 |ref| + 2e-3; fp16 1e-3 |ref| + 1e-5; fp32 1e-5 |ref| + 1e-5;
+ * the zero pattern as for gelu_and_mul_sparse.
+ */
+int gelu_and_mul_sparse_typed(void *out, const void *in, int64_t T, int64_t d,
+                              int64_t row_stride, double z, int dtype,
+                              int variant, int cluster, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -45,7 +45,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for code in range(-8, 1):
+    for code in range(-9, 1):
         s = lib.gated_act_status_string(code)
         assert s and s.decode()
     assert lib.gated_act_status_string(-99).decode() == "unknown status"
@@ -110,9 +110,10 @@ def test_widened_rows_reject_bad_arguments(lib):
     assert lib.squared_relu(0x100000 + 62, 0x100000, 4, 8, None) == ga.ERR_OVERLAP
 
 
-def plan(lib, T, d, rs=None, variant=0, cluster=0, sms=GB300_SMS, out=0x10000, inp=0x100000):
+def plan(lib, T, d, rs=None, variant=0, cluster=0, sms=GB300_SMS, out=0x10000, inp=0x100000,
+         dtype=0):
     p = ga.Plan()
-    rc = lib.gelu_and_mul_sparse_plan(out, inp, T, d, rs or 2 * d, variant, cluster, sms,
+    rc = lib.gelu_and_mul_sparse_plan(out, inp, T, d, rs or 2 * d, dtype, variant, cluster, sms,
                                       ctypes.byref(p))
     return rc, p.as_dict()
 
@@ -181,6 +182,26 @@ def test_plan_tma_rows_limits(lib):
     assert plan(lib, 4096, 31, variant=ga.VARIANT_TMA_ROWS)[0] == ga.ERR_VARIANT
     assert plan(lib, 4096, 64, rs=130, variant=ga.VARIANT_TMA_ROWS)[0] == ga.ERR_VARIANT
     assert plan(lib, 5, 8192, variant=ga.VARIANT_TMA_ROWS)[1]["grid"] == 5
+
+
+def test_plan_typed(lib):
+    # fp16 rows use the CTA-row geometry, fp32 rows hold 4 elements per vector
+    rc, p = plan(lib, 2048, 16384, dtype=ga.F16)
+    assert rc == 0 and p["variant"] == "cta_row" and p["threads"] == 512
+    rc, p = plan(lib, 2048, 16384, dtype=ga.F32)
+    assert rc == 0 and p["variant"] == "cta_row" and p["threads"] == 1024 and p["cluster"] == 1
+    rc, p = plan(lib, 2048, 32768, dtype=ga.F32)
+    assert rc == 0 and p["cluster"] == 2
+    assert plan(lib, 4, 6, dtype=ga.F32)[1]["variant"] == "scalar"      # d not a multiple of 4
+    assert plan(lib, 4, 12, dtype=ga.F32)[1]["variant"] == "cta_row"
+    assert plan(lib, 4, 64, dtype=ga.F16, variant=ga.VARIANT_TMA_ROWS)[0] == ga.ERR_VARIANT
+    assert plan(lib, 4, 64, dtype=ga.F32, variant=ga.VARIANT_WARP_ROWS)[0] == ga.ERR_VARIANT
+    assert plan(lib, 4, 64, dtype=3)[0] == ga.ERR_DTYPE
+    # typed validation: fp32 pointers must be 4-byte aligned
+    assert lib.gelu_and_mul_sparse_typed(0x1002, 0x100000, 4, 8, 16, 1.0, ga.F32, 0, 0,
+                                         None) == ga.ERR_ALIGN
+    assert lib.gelu_and_mul_sparse_typed(0x100000 + 120, 0x100000, 4, 8, 16, 1.0, ga.F32, 0, 0,
+                                         None) == ga.ERR_OVERLAP
 
 
 def test_plan_forced_variants(lib):

@@ -69,26 +69,29 @@ def from_bits(bits: np.ndarray) -> torch.Tensor:
 
 
 def iid(T: int, d: int, seed: int, row_stride: int | None = None,
-        z: float = Z95, name: str = "iid", pad_value: float = math.nan) -> GatedInput:
+        z: float = Z95, name: str = "iid", pad_value: float = math.nan,
+        dtype: torch.dtype = torch.bfloat16) -> GatedInput:
     """Gate and up i.i.d. N(0,1), drawn as one [T, 2d] tensor.
 
     With ``row_stride > 2d`` the extra columns hold ``pad_value`` (NaN by
-    default) so that a stray read of padding poisons the output.
+    default) so that a stray read of padding poisons the output.  ``dtype``
+    is the element type the float32 draws are rounded to (once).
     """
     g = _gen(seed)
     x = torch.randn((T, 2 * d), generator=g, dtype=torch.float32)
-    return GatedInput(name, _pad(x, row_stride, pad_value), d, z, seed)
+    return GatedInput(name, _pad(x, row_stride, pad_value, dtype), d, z, seed)
 
 
-def _pad(x: torch.Tensor, row_stride: int | None, pad_value: float) -> torch.Tensor:
+def _pad(x: torch.Tensor, row_stride: int | None, pad_value: float,
+         dtype: torch.dtype = torch.bfloat16) -> torch.Tensor:
     T, w = x.shape
     if row_stride is None or row_stride == w:
-        return x.to(torch.bfloat16)
+        return x.to(dtype)
     if row_stride < w:
         raise ValueError("row_stride must be >= 2d")
     out = torch.full((T, row_stride), pad_value, dtype=torch.float32)
     out[:, :w] = x
-    return out.to(torch.bfloat16)
+    return out.to(dtype)
 
 
 def tiny() -> GatedInput:
@@ -96,7 +99,7 @@ def tiny() -> GatedInput:
     return iid(TINY_T, TINY_D, seed=0, name="tiny")
 
 
-def decode(T: int, d: int = DECODE_D) -> GatedInput:
+def decode(T: int, d: int = DECODE_D, dtype: torch.dtype = torch.bfloat16) -> GatedInput:
     """Decode rows: d=8192, seed 1000+T.
 
     gate = 0.2 + 1.5 * N(0,1); each gate entry is independently (probability
@@ -110,11 +113,12 @@ def decode(T: int, d: int = DECODE_D) -> GatedInput:
     outl = 8.0 * torch.randn((T, d), generator=g)
     gate = torch.where(sel, outl, gate)
     up = torch.randn((T, d), generator=g)
-    x = torch.cat([gate, up], dim=1).to(torch.bfloat16)
+    x = torch.cat([gate, up], dim=1).to(dtype)
     return GatedInput(f"decode_T{T}", x, d, Z95, seed)
 
 
-def prefill(T: int = PREFILL_T, d: int = PREFILL_D) -> GatedInput:
+def prefill(T: int = PREFILL_T, d: int = PREFILL_D,
+            dtype: torch.dtype = torch.bfloat16) -> GatedInput:
     """Prefill rows: T=2048, d=16384, row_stride 32768 = 2d, seed 2.
 
     gate = s_r * N(0,1) + m_r with per-row scale s_r ~ U(0.5, 2) and shift
@@ -126,7 +130,7 @@ def prefill(T: int = PREFILL_T, d: int = PREFILL_D) -> GatedInput:
     m = -1.0 + 2.0 * torch.rand((T, 1), generator=g)
     gate = s * torch.randn((T, d), generator=g) + m
     up = torch.randn((T, d), generator=g)
-    x = torch.cat([gate, up], dim=1).to(torch.bfloat16)
+    x = torch.cat([gate, up], dim=1).to(dtype)
     return GatedInput("prefill", x, d, Z95, seed)
 
 
@@ -134,7 +138,8 @@ def sweep_seed(T: int, d: int) -> int:
     return 7919 * T + d
 
 
-def sweep(T: int, d: int, z: float = Z95, const_rows: bool = True) -> GatedInput:
+def sweep(T: int, d: int, z: float = Z95, const_rows: bool = True,
+          dtype: torch.dtype = torch.bfloat16) -> GatedInput:
     """Sweep shape (T, d): i.i.d. N(0,1), seed 7919*T + d.
 
     With ``const_rows`` three rows whose gate is all one constant (0, 0.75,
@@ -149,7 +154,7 @@ def sweep(T: int, d: int, z: float = Z95, const_rows: bool = True) -> GatedInput
         up = torch.randn((len(CONST_GATES), d), generator=g)
         gate = torch.tensor(CONST_GATES, dtype=torch.float32)[:, None].expand(-1, d)
         x = torch.cat([x, torch.cat([gate, up], dim=1)], dim=0)
-    return GatedInput(f"sweep_T{T}_d{d}", x.to(torch.bfloat16), d, z, seed)
+    return GatedInput(f"sweep_T{T}_d{d}", x.to(dtype), d, z, seed)
 
 
 def silu(M: int, d: int = SILU_D) -> torch.Tensor:
