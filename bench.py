@@ -96,6 +96,10 @@ def extra_launches() -> list[dict]:
         {"op": "gelu_dense", "T": 64, "d": 8192, "z": None, "bytes": gelu_bytes(64, 8192)},
         {"op": "squared_relu", "T": 2048, "d": d, "z": None, "bytes": 2048 * d * 2 * 2},
         {"op": "squared_relu", "T": 16384, "d": d, "z": None, "bytes": 16384 * d * 2 * 2},
+        {"op": "gelu_f16", "T": 2048, "d": 16384, "z": W.Z95, "bytes": gelu_bytes(2048, 16384)},
+        {"op": "gelu_f32", "T": 2048, "d": 16384, "z": W.Z95,
+         "bytes": 2 * gelu_bytes(2048, 16384)},
+        {"op": "gelu_f32", "T": 64, "d": 8192, "z": W.Z95, "bytes": 2 * gelu_bytes(64, 8192)},
     ]
 
 
@@ -279,12 +283,19 @@ def _launch(ga, L, x, out):
         ga.gelu_and_mul(x, d=L["d"], out=out)
     elif op == "squared_relu":
         ga.squared_relu(x, out=out)
+    elif op in ("gelu_f16", "gelu_f32"):
+        ga.gelu_and_mul_sparse(x, L["z"], d=L["d"], out=out)
     else:
         raise ValueError(op)
 
 
 def _in_width(L) -> int:
     return L["d"] if L["op"] == "squared_relu" else 2 * L["d"]
+
+
+def _dtype_of(L):
+    import torch
+    return {"gelu_f16": torch.float16, "gelu_f32": torch.float32}.get(L["op"], torch.bfloat16)
 
 
 def per_shape_times(ga, launches, dev, peak_gbs, reps=5) -> tuple[list, float]:
@@ -328,14 +339,16 @@ def per_shape_times(ga, launches, dev, peak_gbs, reps=5) -> tuple[list, float]:
         T, d = L["T"], L["d"]
         if L["op"] == "silu_bounded":
             L["n_rows"] = torch.tensor([L["live"]], dtype=torch.int32, device=dev)
+        dt = _dtype_of(L)
+        a_in, a_out = arena_in.view(dt), arena_out.view(dt)     # same bytes, reinterpreted
         n_in, n_out = T * _in_width(L), T * d
-        win = max(1, min(arena_in.numel() // n_in, arena_out.numel() // n_out))
+        win = max(1, min(a_in.numel() // n_in, a_out.numel() // n_out))
         N = int(min(200, max(20, win)))
         fns = []
         for i in range(N):
             w = i % win
-            x = arena_in[w * n_in:(w + 1) * n_in].view(T, _in_width(L))
-            o = arena_out[w * n_out:(w + 1) * n_out].view(T, d)
+            x = a_in[w * n_in:(w + 1) * n_in].view(T, _in_width(L))
+            o = a_out[w * n_out:(w + 1) * n_out].view(T, d)
             fns.append(lambda x=x, o=o, L=L: _launch(ga, L, x, o))
         t = timed_graph(fns)
         seen[key] = t
