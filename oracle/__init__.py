@@ -80,6 +80,14 @@ class Oracle:
             ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
             ctypes.c_double, _c_double_p, _c_u8_p, _c_double_p, _c_double_p, _c_double_p,
             ctypes.c_int]
+        lib.oracle_round_f16.restype = ctypes.c_double
+        lib.oracle_round_f16.argtypes = [ctypes.c_double]
+        lib.oracle_round_bf16.restype = ctypes.c_double
+        lib.oracle_round_bf16.argtypes = [ctypes.c_double]
+        lib.oracle_gelu_and_mul_sparse_native.restype = ctypes.c_int
+        lib.oracle_gelu_and_mul_sparse_native.argtypes = [
+            ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+            ctypes.c_double, _c_double_p, _c_u8_p, _c_double_p, ctypes.c_int]
         lib.oracle_squared_relu.restype = ctypes.c_double
         lib.oracle_squared_relu.argtypes = [ctypes.c_double]
         lib.oracle_gelu_and_mul.restype = ctypes.c_int
@@ -165,6 +173,35 @@ class Oracle:
         if rc != 0:
             raise ValueError(f"oracle_gelu_and_mul_sparse_typed rejected T={T} d={d} rs={rs}")
         return GeluSparseResult(ref, mask.astype(bool), mean, std, cutoff)
+
+    def round_f16(self, v: float) -> float:
+        return self._lib.oracle_round_f16(float(v))
+
+    def round_bf16(self, v: float) -> float:
+        return self._lib.oracle_round_bf16(float(v))
+
+    def gelu_and_mul_sparse_native(self, x: np.ndarray, d: int, z: float, bf16_bits: bool = False,
+                                   nthreads: int = 0) -> tuple[np.ndarray, np.ndarray, np.ndarray]:
+        """Native-rounding gelu_and_mul_sparse on bf16 bit patterns (uint16 with
+        bf16_bits=True) or float16 values.  Returns (out already rounded to the
+        element type, as float64 [T, d]; mask g > c [T, d]; cutoff c [T])."""
+        a = np.ascontiguousarray(x)
+        if a.dtype == np.uint16 and bf16_bits:
+            code = 0
+        elif a.dtype == np.float16:
+            code = 1
+        else:
+            raise ValueError("native rounding takes bf16 bit patterns or float16 values")
+        T, rs = a.shape
+        ref = np.empty((T, d), dtype=np.float64)
+        mask = np.empty((T, d), dtype=np.uint8)
+        cutoff = np.empty(T, dtype=np.float64)
+        rc = self._lib.oracle_gelu_and_mul_sparse_native(
+            a.ctypes.data_as(ctypes.c_void_p), code, T, d, rs, float(z), _ptr(ref, _c_double_p),
+            _ptr(mask, _c_u8_p), _ptr(cutoff, _c_double_p), int(nthreads))
+        if rc != 0:
+            raise ValueError(f"oracle_gelu_and_mul_sparse_native rejected T={T} d={d} rs={rs}")
+        return ref, mask.astype(bool), cutoff
 
     def silu_and_mul(self, in_bits: np.ndarray, d: int | None = None,
                      nthreads: int = 0) -> tuple[np.ndarray, np.ndarray]:

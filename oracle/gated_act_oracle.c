@@ -235,6 +235,95 @@ int oracle_gelu_and_mul_sparse(const uint16_t *in, int64_t T, int64_t d,
                                             row_mean, row_std, row_cutoff, nthreads);
 }
 
+/*
+ * Round a double to the nearest IEEE binary16 value (ties to even, gradual
+ * underflow, overflow to infinity) and return that value as a double.  Same
+ * method as the bf16 encoder: the quantum of |v|'s binade is 2^(e-10), fixed
+ * at 2^-24 below the smallest normal 2^-14.
+ */
+double oracle_round_f16(double v)
+{
+    if (isnan(v) || v == 0.0)
+        return v;
+    double a = fabs(v);
+    if (isinf(a) || a >= 65520.0)      /* halfway between 65504 and 2^16 rounds up */
+        return copysign(INFINITY, v);
+    int e2;
+    frexp(a, &e2);
+    int e = e2 - 1;
+    if (e < -14)
+        e = -14;
+    double q = ldexp(1.0, e - 10);
+    return copysign(rint(a / q) * q, v);
+}
+
+/* Round a double to the nearest bf16 value, returned as a double. */
+double oracle_round_bf16(double v)
+{
+    return oracle_bf16_to_double(oracle_double_to_bf16(v));
+}
+
+/*
+ * gelu_and_mul_sparse in native-rounding mode: the op as a composition of
+ * separate element-type ops, as the sparse-GELU page's kernel reproduces
+ * native PyTorch ("Cross-architecture warp and dtype validation":
+ * input-dtype roundtrips at operation boundaries).  Each op of an element
+ * type is computed in binary32 and its result rounded to the element type
+ * (bf16 or fp16), so a boundary is R(x) = round_T(round_binary32(x)) with x
+ * the op's exact value -- two roundings, which differ from one when the
+ * binary32 result lands on a midpoint of the element type.  Boundaries:
+ *   m = R(mean g),  sd = R(population std g)  (std from the exact mean),
+ *   t = R(sd * zf)  with zf = z rounded to binary32 (a scalar operand),
+ *   c = R(m + t),   s = max(R(g - c), 0),  a = R(gelu_tanh(s)),  out = R(a * u).
+ * ref holds out (already rounded); mask is g > c; row_cutoff holds c.
+ */
+int oracle_gelu_and_mul_sparse_native(const void *in, int dtype, int64_t T, int64_t d,
+                                      int64_t row_stride, double z, double *ref,
+                                      uint8_t *mask, double *row_cutoff, int nthreads)
+{
+    if (T < 0 || d <= 0 || row_stride < 2 * d ||
+        (dtype != ORACLE_BF16 && dtype != ORACLE_F16))
+        return -1;
+    double (*RT)(double) = dtype == ORACLE_F16 ? oracle_round_f16 : oracle_round_bf16;
+#define R(x) RT((double)(float)(x))
+    const double zf = (double)(float)z;
+    set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < T; ++r) {
+        const int64_t g0 = r * row_stride, u0 = g0 + d;
+
+        double sum = 0.0;
+        for (int64_t j = 0; j < d; ++j)
+            sum += load_elem(in, dtype, g0 + j);
+        const double mean = sum / (double)d;
+        double ss = 0.0;
+        for (int64_t j = 0; j < d; ++j) {
+            double dev = load_elem(in, dtype, g0 + j) - mean;
+            ss += dev * dev;
+        }
+        const double m = R(mean);
+        const double sd = R(sqrt(ss / (double)d));
+        const double t = R(sd * zf);
+        const double c = R(m + t);
+
+        for (int64_t j = 0; j < d; ++j) {
+            double g = load_elem(in, dtype, g0 + j);
+            double u = load_elem(in, dtype, u0 + j);
+            double s = R(g - c);
+            if (s < 0.0)
+                s = 0.0;
+            double a = R(oracle_gelu_tanh(s));
+            ref[r * d + j] = R(a * u);
+            if (mask)
+                mask[r * d + j] = (uint8_t)(g > c);
+        }
+        if (row_cutoff)
+            row_cutoff[r] = c;
+    }
+#undef R
+    return 0;
+}
+
 /* squared ReLU, in double. */
 double oracle_squared_relu(double x)
 {

@@ -377,3 +377,57 @@ def test_typed_worked_example_fp32(oracle):
     res = oracle.gelu_and_mul_sparse_typed(x, d=2, z=0.5)
     g05 = F.gelu(torch.tensor(0.5, dtype=torch.float64), approximate="tanh").item()
     assert res.ref[0, 0] == 0.0 and res.ref[0, 1] == pytest.approx(-2.0 * g05, rel=1e-15)
+
+
+# ---------------------------------------------------------------- native-rounding mode
+def test_round_f16_matches_numpy(oracle):
+    rng = np.random.default_rng(8)
+    v = np.concatenate([rng.standard_normal(20000) * 10.0 ** rng.integers(-9, 5, 20000),
+                        [65504.0, 65519.9, 65520.0, 6e-8, 3e-8, 2.98e-8, -1e-9, 0.0]])
+    # numpy rounds float64 -> float16 directly (one rounding); the values past
+    # 65520 overflow to infinity on purpose
+    with np.errstate(over="ignore"):
+        want = v.astype(np.float16).astype(np.float64)
+    got = np.array([oracle.round_f16(x) for x in v])
+    assert np.array_equal(got, want)
+
+
+def test_native_mode_against_torch_cpu_composition(oracle):
+    # The native-rounding oracle (each op exact, rounded to the element type)
+    # against torch's own CPU composition of the separate ops in that type.
+    # fp32 accumulation order in torch's mean/std can move a rounded statistic
+    # by one step on rare rows; everywhere else the two agree exactly.
+    for dt in (torch.bfloat16, torch.float16):
+        x = W.prefill(T=48, d=4096, dtype=dt).x
+        g, u = x[:, :4096], x[:, 4096:]
+        m = g.mean(dim=1, keepdim=True)
+        sd = g.std(dim=1, keepdim=True, unbiased=False)
+        c = m + sd * Z95
+        want = (F.gelu(torch.relu(g - c), approximate="tanh") * u).to(torch.float64).numpy()
+        arr = W.to_bits(x) if dt == torch.bfloat16 else x.numpy()
+        ref, mask, cut = oracle.gelu_and_mul_sparse_native(arr, d=4096, z=Z95,
+                                                           bf16_bits=dt == torch.bfloat16)
+        same_rows = cut == c.to(torch.float64).numpy()[:, 0]
+        assert same_rows.mean() >= 0.95
+        # where the rounded cutoff agrees, every element agrees bit for bit
+        assert np.array_equal(ref[same_rows], want[same_rows])
+
+
+def test_native_mode_worked_example(oracle):
+    # gate [1, 3], up [7, -2], z = 0.5 in bf16: m = 2, sd = 1, t = R(0.5) = 0.5,
+    # c = 2.5; s = R(3 - 2.5) = 0.5; a = R(gelu(0.5)) ; out = R(a * -2)
+    x = torch.tensor([[1.0, 3.0, 7.0, -2.0]], dtype=torch.bfloat16)
+    ref, mask, cut = oracle.gelu_and_mul_sparse_native(W.to_bits(x), d=2, z=0.5, bf16_bits=True)
+    a = torch.tensor(F.gelu(torch.tensor(0.5, dtype=torch.float64), approximate="tanh").item(),
+                     dtype=torch.float64).to(torch.bfloat16).to(torch.float64).item()
+    want = torch.tensor(a * -2.0, dtype=torch.float64).item()
+    assert cut[0] == 2.5 and ref[0, 0] == 0.0 and list(mask[0]) == [False, True]
+    assert ref[0, 1] == oracle.round_bf16(want)
+
+
+def test_native_mode_rounds_the_statistics(oracle):
+    # a row whose exact mean is not a bf16 number: the cutoff must be built
+    # from the rounded mean (0.333... -> 0.333984375), not the exact one
+    x = torch.tensor([[0.0, 0.0, 1.0, 1.0, 1.0, 1.0]], dtype=torch.bfloat16)
+    ref, mask, cut = oracle.gelu_and_mul_sparse_native(W.to_bits(x), d=3, z=0.0, bf16_bits=True)
+    assert cut[0] == oracle.round_bf16(1.0 / 3.0) == 0.333984375
