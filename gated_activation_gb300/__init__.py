@@ -29,7 +29,8 @@ VARIANT_AUTO, VARIANT_WARP_ROWS, VARIANT_CTA_ROW, VARIANT_SCALAR, VARIANT_TMA_RO
 VARIANT_NAMES = {0: "auto", 1: "warp_rows", 2: "cta_row", 3: "scalar", 4: "tma_rows"}
 
 EXPORTED = (
-    "gelu_and_mul_sparse", "gelu_and_mul_sparse_typed", "silu_and_mul", "gated_act_status_string",
+    "gelu_and_mul_sparse", "gelu_and_mul_sparse_typed", "gelu_and_mul_sparse_native",
+    "silu_and_mul", "gated_act_status_string",
     "gated_act_last_cuda_error", "gelu_and_mul_sparse_plan", "gelu_and_mul_sparse_ex",
     "gated_act_device_status", "gated_act_noop", "silu_and_mul_bounded", "gelu_and_mul",
     "squared_relu",
@@ -84,6 +85,9 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.gelu_and_mul_sparse_typed.argtypes = [vp, cvp, i64, i64, i64, ctypes.c_double,
                                               ctypes.c_int, ctypes.c_int, ctypes.c_int, vp]
     lib.gelu_and_mul_sparse_typed.restype = ctypes.c_int
+    lib.gelu_and_mul_sparse_native.argtypes = [vp, cvp, i64, i64, i64, ctypes.c_double,
+                                               ctypes.c_int, vp]
+    lib.gelu_and_mul_sparse_native.restype = ctypes.c_int
     lib.gelu_and_mul_sparse_plan.restype = ctypes.c_int
     lib.silu_and_mul.argtypes = [vp, cvp, i64, i64, vp]
     lib.silu_and_mul.restype = ctypes.c_int
@@ -161,6 +165,29 @@ def gelu_and_mul_sparse(x: torch.Tensor, z: float, d: int | None = None,
                                        _DTYPE_CODE[x.dtype], int(variant), int(cluster),
                                        _stream_handle(stream))
     _check("gelu_and_mul_sparse", rc)
+    return out
+
+
+def gelu_and_mul_sparse_native(x: torch.Tensor, z: float, d: int | None = None,
+                               out: torch.Tensor | None = None,
+                               stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """Native-rounding sparse GELU of ``x`` ([T, >=2d] bf16 or fp16 CUDA): every
+    intermediate rounded to the element type, as separate PyTorch ops round."""
+    T, rs = _rows_view(x, (torch.bfloat16, torch.float16))
+    if d is None:
+        if x.shape[1] % 2:
+            raise ValueError("odd row length: pass d explicitly")
+        d = int(x.shape[1]) // 2
+    if x.shape[1] < 2 * d:
+        raise ValueError("rows are shorter than 2d")
+    if out is None:
+        out = torch.empty((T, d), dtype=x.dtype, device=x.device)
+    elif out.shape != (T, d) or out.dtype != x.dtype or not out.is_contiguous():
+        raise ValueError(f"out must be a contiguous [T, d] {x.dtype} tensor")
+    rc = load_library().gelu_and_mul_sparse_native(out.data_ptr(), x.data_ptr(), T, d, rs,
+                                                   float(z), _DTYPE_CODE[x.dtype],
+                                                   _stream_handle(stream))
+    _check("gelu_and_mul_sparse_native", rc)
     return out
 
 
@@ -270,6 +297,6 @@ def squared_relu(x: torch.Tensor, out: torch.Tensor | None = None,
     return out
 
 
-__all__ = ["silu_and_mul_bounded", "gelu_and_mul", "squared_relu", "gelu_and_mul_sparse", "gelu_and_mul_sparse_plan", "silu_and_mul", "device_status", "noop",
+__all__ = ["gelu_and_mul_sparse_native", "silu_and_mul_bounded", "gelu_and_mul", "squared_relu", "gelu_and_mul_sparse", "gelu_and_mul_sparse_plan", "silu_and_mul", "device_status", "noop",
            "load_library",
            "status_string", "GatedActError", "Plan", "EXPORTED", "LIB_PATH"]

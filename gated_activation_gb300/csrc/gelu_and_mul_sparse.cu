@@ -184,6 +184,48 @@ __device__ __forceinline__ uint4 epi_vec(const uint4 &g, const uint4 &u, float c
     return o;
 }
 
+// Round an fp32 value to the format and back (nearest even).
+template <class F> __device__ __forceinline__ float round_t(float x);
+template <> __device__ __forceinline__ float round_t<FmtBf16>(float x) {
+    return __bfloat162float(__float2bfloat16_rn(x));
+}
+template <> __device__ __forceinline__ float round_t<FmtF16>(float x) {
+    return __half2float(__float2half_rn(x));
+}
+template <> __device__ __forceinline__ float round_t<FmtF32>(float x) { return x; }
+
+// Native-rounding epilogue: each op of the composition computed in fp32 and
+// rounded to the format -- s = R(g - c), relu, a = R(gelu_tanh(s)) with an
+// accurate tanh, out = R(a * u).
+template <class F>
+__device__ __forceinline__ float native_gelu_mul(float g, float u, float c) {
+    const float s = relu_nan(round_t<F>(g - c));
+    const float y = kSqrt2OverPi * (s + 0.044715f * s * s * s);
+    const float a = round_t<F>(0.5f * s * (1.0f + tanhf(y)));
+    return a * u;   // rounded by put_pair
+}
+
+template <class F>
+__device__ __forceinline__ uint4 epi_vec_native(const uint4 &g, const uint4 &u, float cutoff) {
+    uint4 o;
+#pragma unroll
+    for (int i = 0; i < F::kPairs; ++i) {
+        const float2 gp = F::pair(g, i), up = F::pair(u, i);
+        F::put_pair(o, i, make_float2(native_gelu_mul<F>(gp.x, up.x, cutoff),
+                                      native_gelu_mul<F>(gp.y, up.y, cutoff)));
+    }
+    return o;
+}
+
+// The native composition's cutoff from the fp32 row statistics:
+// c = R(R(mean) + R(R(std) * z)).
+template <class F>
+__device__ __forceinline__ float native_cutoff(float mean, float var, float z) {
+    const float m = round_t<F>(mean);
+    const float sd = round_t<F>(__fsqrt_rn(var));
+    return round_t<F>(m + round_t<F>(sd * z));
+}
+
 // Running pair sums over one vector of gate values.
 template <class F>
 __device__ __forceinline__ float2 sum_vec(float2 acc, const uint4 &g) {
@@ -453,7 +495,9 @@ gelu_warp_rows(uint16_t *__restrict__ out, const uint16_t *__restrict__ in, int6
 // thread t the vectors k sv + t + NT i.  Rows advance by the number of
 // clusters in the grid.  CL = false: C must be 1 (no cluster code is
 // compiled in).  F is the element format.
-template <int NT, int V, bool CL, class F>
+// NATIVE: the native-rounding composition (cutoff and epilogue rounded to the
+// format after every op).
+template <int NT, int V, bool CL, class F, bool NATIVE>
 __global__ void __launch_bounds__(NT, (1024 / NT) > 0 ? (1024 / NT) : 1)
 gelu_cta_rows(void *__restrict__ out_, const void *__restrict__ in_, int64_t T, int d,
               int64_t rs, float z, int C, int sv) {
@@ -543,15 +587,16 @@ gelu_cta_rows(void *__restrict__ out_, const void *__restrict__ in_, int64_t T, 
             var = __fdiv_rn(warp_sum(q_k + between), static_cast<float>(d));
             cluster_arrive_release();   // this CTA is done reading its peers
         }
-        const float sd = __fsqrt_rn(var);
-        const float cutoff = fmaf(sd, z, mean);
+        const float cutoff = NATIVE ? native_cutoff<F>(mean, var, z)
+                                    : fmaf(__fsqrt_rn(var), z, mean);
 
         uint8_t *op = out + row * d_bytes;
 #pragma unroll
         for (int i = 0; i < V; ++i) {
             const int v = v0 + tid + NT * i;
             if (v < v1)
-                st_vec(op + 16 * v, epi_vec<F>(g[i], u[i], cutoff));
+                st_vec(op + 16 * v, NATIVE ? epi_vec_native<F>(g[i], u[i], cutoff)
+                                           : epi_vec<F>(g[i], u[i], cutoff));
         }
         if (CL)
             cluster_wait_acquire();   // peers are done with xch before it changes
@@ -568,7 +613,7 @@ __device__ __forceinline__ float sparse_gelu_mul(float g, float u, float cutoff,
     return fmaf(h, exact_tanh ? tanhf(y) : tanh_approx(y), h) * u;
 }
 
-template <class F>
+template <class F, bool NATIVE>
 __global__ void __launch_bounds__(kScalarThreads)
 gelu_scalar_rows(void *__restrict__ out_, const void *__restrict__ in_, int64_t T, int64_t d,
                  int64_t rs, float z) {
@@ -594,12 +639,15 @@ gelu_scalar_rows(void *__restrict__ out_, const void *__restrict__ in_, int64_t 
             q = fmaf(e, e, q);
         }
         q = block_sum<NW>(q, red[1], lane, warp);
-        const float sd = __fsqrt_rn(__fdiv_rn(q, static_cast<float>(d)));
-        const float cutoff = fmaf(sd, z, mean);
+        const float var = __fdiv_rn(q, static_cast<float>(d));
+        const float cutoff = NATIVE ? native_cutoff<F>(mean, var, z)
+                                    : fmaf(__fsqrt_rn(var), z, mean);
         uint8_t *op = out + row * d * E;
-        for (int64_t j = tid; j < d; j += kScalarThreads)
-            F::store1(op + j * E, sparse_gelu_mul(F::load1(gp + j * E), F::load1(up + j * E),
-                                                  cutoff, E == 4));
+        for (int64_t j = tid; j < d; j += kScalarThreads) {
+            const float g = F::load1(gp + j * E), u = F::load1(up + j * E);
+            F::store1(op + j * E, NATIVE ? native_gelu_mul<F>(g, u, cutoff)
+                                         : sparse_gelu_mul(g, u, cutoff, E == 4));
+        }
     }
 }
 
@@ -619,46 +667,53 @@ WarpFn warp_fn(int v) {
     }
 }
 
-template <bool CL, class F>
+template <bool CL, class F, bool N>
 CtaFn cta_fn_t(int nt, int v) {
     if (v == 2) {
         switch (nt) {
-        case 64: return gelu_cta_rows<64, 2, CL, F>;
-        case 128: return gelu_cta_rows<128, 2, CL, F>;
+        case 64: return gelu_cta_rows<64, 2, CL, F, N>;
+        case 128: return gelu_cta_rows<128, 2, CL, F, N>;
         default: return nullptr;
         }
     }
     if (v == 4) {
         switch (nt) {
-        case 64: return gelu_cta_rows<64, 4, CL, F>;
-        case 128: return gelu_cta_rows<128, 4, CL, F>;
-        case 256: return gelu_cta_rows<256, 4, CL, F>;
-        case 512: return gelu_cta_rows<512, 4, CL, F>;
-        case 1024: return gelu_cta_rows<1024, 4, CL, F>;
+        case 64: return gelu_cta_rows<64, 4, CL, F, N>;
+        case 128: return gelu_cta_rows<128, 4, CL, F, N>;
+        case 256: return gelu_cta_rows<256, 4, CL, F, N>;
+        case 512: return gelu_cta_rows<512, 4, CL, F, N>;
+        case 1024: return gelu_cta_rows<1024, 4, CL, F, N>;
         default: return nullptr;
         }
     }
     return nullptr;
 }
 
-template <class F>
+template <class F, bool N>
 CtaFn cta_fn_f(int nt, int v, int cluster) {
-    return cluster > 1 ? cta_fn_t<true, F>(nt, v) : cta_fn_t<false, F>(nt, v);
+    return cluster > 1 ? cta_fn_t<true, F, N>(nt, v) : cta_fn_t<false, F, N>(nt, v);
 }
 
-CtaFn cta_fn(int nt, int v, int cluster, int dtype) {
+// native: the native-rounding composition (bf16 and fp16 only)
+CtaFn cta_fn(int nt, int v, int cluster, int dtype, bool native) {
     switch (dtype) {
-    case GATED_ACT_F16: return cta_fn_f<FmtF16>(nt, v, cluster);
-    case GATED_ACT_F32: return cta_fn_f<FmtF32>(nt, v, cluster);
-    default: return cta_fn_f<FmtBf16>(nt, v, cluster);
+    case GATED_ACT_F16:
+        return native ? cta_fn_f<FmtF16, true>(nt, v, cluster)
+                      : cta_fn_f<FmtF16, false>(nt, v, cluster);
+    case GATED_ACT_F32: return native ? nullptr : cta_fn_f<FmtF32, false>(nt, v, cluster);
+    default:
+        return native ? cta_fn_f<FmtBf16, true>(nt, v, cluster)
+                      : cta_fn_f<FmtBf16, false>(nt, v, cluster);
     }
 }
 
-ScalarFn scalar_fn(int dtype) {
+ScalarFn scalar_fn(int dtype, bool native) {
     switch (dtype) {
-    case GATED_ACT_F16: return gelu_scalar_rows<FmtF16>;
-    case GATED_ACT_F32: return gelu_scalar_rows<FmtF32>;
-    default: return gelu_scalar_rows<FmtBf16>;
+    case GATED_ACT_F16:
+        return native ? gelu_scalar_rows<FmtF16, true> : gelu_scalar_rows<FmtF16, false>;
+    case GATED_ACT_F32: return native ? nullptr : gelu_scalar_rows<FmtF32, false>;
+    default:
+        return native ? gelu_scalar_rows<FmtBf16, true> : gelu_scalar_rows<FmtBf16, false>;
     }
 }
 
@@ -687,8 +742,9 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 struct Plan {
     gated_act_plan pub;
-    int sv;      // vectors per CTA slice (CTA rows)
-    int dtype;   // gated_act_dtype of in and out
+    int sv;        // vectors per CTA slice (CTA rows)
+    int dtype;     // gated_act_dtype of in and out
+    bool native;   // native-rounding composition
 };
 
 // Threads and vectors per thread for a CTA slice of sv vectors.
@@ -767,8 +823,9 @@ int validate(const void *out, const void *in, int64_t T, int64_t d, int64_t rs, 
 }
 
 int make_plan(const void *out, const void *in, int64_t T, int64_t d, int64_t rs, int dtype,
-              int variant, int cluster, int sm_count, bool check_ptrs, Plan *p) {
-    if (dtype < GATED_ACT_BF16 || dtype > GATED_ACT_F32)
+              int variant, int cluster, int sm_count, bool check_ptrs, Plan *p,
+              bool native = false) {
+    if (dtype < GATED_ACT_BF16 || dtype > GATED_ACT_F32 || (native && dtype == GATED_ACT_F32))
         return GATED_ACT_ERR_DTYPE;
     const int elem = elem_bytes(dtype), epv = 16 / elem;
     const int rc = validate(out, in, T, d, rs, elem, check_ptrs);
@@ -776,21 +833,23 @@ int make_plan(const void *out, const void *in, int64_t T, int64_t d, int64_t rs,
         return rc;
     if (variant < GATED_ACT_VARIANT_AUTO || variant > GATED_ACT_VARIANT_TMA_ROWS)
         return GATED_ACT_ERR_VARIANT;
-    // the warp-rows and TMA-rows kernels exist for bf16 only
-    if (dtype != GATED_ACT_BF16 &&
+    // the warp-rows and TMA-rows kernels exist for plain bf16 only
+    const bool cta_only = dtype != GATED_ACT_BF16 || native;
+    if (cta_only &&
         (variant == GATED_ACT_VARIANT_WARP_ROWS || variant == GATED_ACT_VARIANT_TMA_ROWS))
         return GATED_ACT_ERR_VARIANT;
     gated_act_plan &q = p->pub;
     q = gated_act_plan{};
     p->sv = 0;
     p->dtype = dtype;
+    p->native = native;
     const bool vec_ok = aligned(in, 16) && aligned(out, 16) && d % epv == 0 && rs % epv == 0;
     const int64_t nvec = d / epv;
     const int sms = sm_count > 0 ? sm_count : (T > 0 ? device_sm_count() : 1);
     int t_cps = 0, t_nt = 0, t_stages = 0;
     int64_t t_smem = 0;
     const int want_cps = variant == GATED_ACT_VARIANT_TMA_ROWS ? cluster : 0;
-    const bool tma_ok = vec_ok && dtype == GATED_ACT_BF16 &&
+    const bool tma_ok = vec_ok && !cta_only &&
                         tma_shape(nvec, want_cps, &t_cps, &t_nt, &t_stages, &t_smem);
 
     // Measured on GB300 (every geometry timed per T x d, graph-replayed over
@@ -803,7 +862,7 @@ int make_plan(const void *out, const void *in, int64_t T, int64_t d, int64_t rs,
             variant = GATED_ACT_VARIANT_SCALAR;
         else if (tma_ok && ((nvec >= 4096 && T >= 3 * sm) || (nvec >= 2048 && T >= 12 * sm)))
             variant = GATED_ACT_VARIANT_TMA_ROWS;
-        else if (nvec <= 64 && dtype == GATED_ACT_BF16)
+        else if (nvec <= 64 && !cta_only)
             variant = GATED_ACT_VARIANT_WARP_ROWS;
         else
             variant = GATED_ACT_VARIANT_CTA_ROW;
@@ -929,7 +988,7 @@ int launch(const Plan &p, void *out, const void *in, int64_t T, int64_t d, int64
         e = launch_kernel(warp_fn(q.vec_per_thread), grid, block, 0, stream, 1, o, x, T, di, rs, zf);
         break;
     case GATED_ACT_VARIANT_CTA_ROW: {
-        CtaFn fn = cta_fn(q.threads, q.vec_per_thread, q.cluster, p.dtype);
+        CtaFn fn = cta_fn(q.threads, q.vec_per_thread, q.cluster, p.dtype, p.native);
         if (!fn)
             return GATED_ACT_ERR_VARIANT;
         e = launch_kernel(fn, grid, block, 0, stream, q.cluster, out, in, T, di, rs, zf,
@@ -937,7 +996,8 @@ int launch(const Plan &p, void *out, const void *in, int64_t T, int64_t d, int64
         break;
     }
     default:
-        e = launch_kernel(scalar_fn(p.dtype), grid, block, 0, stream, 1, out, in, T, d, rs, zf);
+        e = launch_kernel(scalar_fn(p.dtype, p.native), grid, block, 0, stream, 1, out, in, T, d,
+                          rs, zf);
         break;
     }
     if (e != cudaSuccess)
@@ -968,6 +1028,17 @@ extern "C" int gelu_and_mul_sparse_typed(void *out, const void *in, int64_t T, i
     gact::Plan p;
     const int rc =
         gact::make_plan(out, in, T, d, row_stride, dtype, variant, cluster, 0, true, &p);
+    if (rc != GATED_ACT_OK || T == 0)
+        return rc;
+    return gact::launch(p, out, in, T, d, row_stride, z, stream);
+}
+
+extern "C" int gelu_and_mul_sparse_native(void *out, const void *in, int64_t T, int64_t d,
+                                          int64_t row_stride, double z, int dtype,
+                                          cudaStream_t stream) {
+    gact::Plan p;
+    const int rc = gact::make_plan(out, in, T, d, row_stride, dtype, GATED_ACT_VARIANT_AUTO, 0,
+                                   0, true, &p, true);
     if (rc != GATED_ACT_OK || T == 0)
         return rc;
     return gact::launch(p, out, in, T, d, row_stride, z, stream);

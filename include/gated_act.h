@@ -248,6 +248,25 @@ int gelu_and_mul_sparse_typed(void *out, const void *in, int64_t T, int64_t d,
                               int64_t row_stride, double z, int dtype,
                               int variant, int cluster, cudaStream_t stream);
 
+/*
+ * gelu_and_mul_sparse in native-rounding mode: the op computed as the
+ * composition of separate element-type ops does it, every intermediate
+ * rounded to the element type.  This is what the sparse-GELU page's kernel
+ * does to reproduce native PyTorch ("Cross-architecture warp and dtype
+ * validation": input-dtype roundtrips at operation boundaries).  Each op
+ * runs in fp32 and its result is rounded (nearest even) to the element type:
+ *   m = R(mean g), sd = R(population std g), t = R(sd * z), c = R(m + t),
+ *   s = relu(R(g - c)), a = R(gelu_tanh(s)), out = R(a * u).
+ *   dtype  GATED_ACT_BF16 or GATED_ACT_F16 (fp32 ops round to fp32 anyway:
+ *          GATED_ACT_ERR_DTYPE).  Other arguments as gelu_and_mul_sparse.
+ * Accuracy: the zero pattern is exactly {g > c}; where the kernel's fp32 row
+ * statistics round to the same c as an exact evaluation (all but rare rows),
+ * each output is within one element-type ulp of that evaluation.
+ */
+int gelu_and_mul_sparse_native(void *out, const void *in, int64_t T, int64_t d,
+                               int64_t row_stride, double z, int dtype,
+                               cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

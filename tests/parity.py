@@ -114,3 +114,37 @@ def check_silu(out: torch.Tensor, ref16: np.ndarray, label: str = "") -> int:
     mx = int(dist.max()) if dist.size else 0
     assert mx <= 1, f"{label}: {int((dist > 1).sum())} elements more than 1 ulp away (max {mx})"
     return mx
+
+
+def ulp_of(c: np.ndarray, dtype: torch.dtype) -> np.ndarray:
+    """Spacing of the element type at |c| (bf16: 8 significant bits, fp16: 11)."""
+    if dtype == torch.float16:
+        return np.spacing(np.abs(c).astype(np.float16)).astype(np.float64)
+    return np.spacing(np.abs(c).astype(np.float32)).astype(np.float64) * 2.0 ** 16
+
+
+def check_native(out: torch.Tensor, x: torch.Tensor, d: int, ref: np.ndarray, mask: np.ndarray,
+                 cut: np.ndarray, label: str = "") -> dict:
+    """Native-rounding acceptance: outside one rounding step of the row's cutoff
+    the zero pattern equals {g > c} exactly; every output is within one
+    element-type ulp of the (already rounded) oracle value."""
+    dt = out.dtype
+    y = f64_of(out)
+    xf = f64_of(x)
+    g, u = xf[:, :d], xf[:, d:2 * d]
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(y), nan), f"{label}: NaN pattern differs"
+    near = np.abs(g - cut[:, None]) <= ulp_of(cut, dt)[:, None]
+    expect_nz = mask & (ref != 0)
+    flips = ~nan & ((y != 0) != expect_nz)
+    bad_mask = flips & ~near
+    assert not bad_mask.any(), f"{label}: {bad_mask.sum()} zero-pattern mismatches away from c"
+    yb = out.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    rb = torch.from_numpy(ref).to(dt).view(torch.int16).numpy().view(np.uint16)
+    dist = np.abs(ordered(yb) - ordered(rb))
+    bad = ~nan & ~flips & (dist > 1)
+    if bad.any():
+        r, c = np.argwhere(bad)[0]
+        raise AssertionError(f"{label}: {bad.sum()} outputs more than 1 ulp away; first ({r},{c}) "
+                             f"out={y[r, c]!r} ref={ref[r, c]!r}")
+    return {"flips_near_cutoff": int(flips.sum()), "ulp1": int((~nan & (dist == 1)).sum())}

@@ -204,6 +204,14 @@ def test_plan_typed(lib):
                                          None) == ga.ERR_OVERLAP
 
 
+def test_native_rounding_rejects_fp32_and_bad_args(lib):
+    assert lib.gelu_and_mul_sparse_native(0x1000, 0x100000, 4, 8, 16, 1.0, ga.F32,
+                                          None) == ga.ERR_DTYPE
+    assert lib.gelu_and_mul_sparse_native(0x1000, 0x100000, 4, 8, 15, 1.0, ga.BF16,
+                                          None) == ga.ERR_STRIDE
+    assert lib.gelu_and_mul_sparse_native(None, None, 0, 8, 16, 1.0, ga.F16, None) == ga.OK
+
+
 def test_plan_forced_variants(lib):
     assert plan(lib, 4, 2048, variant=ga.VARIANT_CTA_ROW, cluster=2)[1]["cluster"] == 2
     assert plan(lib, 4, 4096, variant=ga.VARIANT_WARP_ROWS)[0] == ga.ERR_VARIANT
