@@ -84,7 +84,8 @@ def workload_launches(only: tuple | None = None) -> list[dict]:
 def extra_launches() -> list[dict]:
     """Widened rows, measured per shape (not part of the timed step): the
     bounded silu at the MoE page's case (a 16384-row buffer bound with 2048
-    live rows, and fully live), dense gelu_and_mul and squared_relu."""
+    live rows, and fully live), dense gelu_and_mul, squared_relu, the sparse
+    GELU on fp16/fp32 rows and in native-rounding mode."""
     import workloads as W
     d = W.SILU_D
     return [
@@ -100,6 +101,9 @@ def extra_launches() -> list[dict]:
         {"op": "gelu_f32", "T": 2048, "d": 16384, "z": W.Z95,
          "bytes": 2 * gelu_bytes(2048, 16384)},
         {"op": "gelu_f32", "T": 64, "d": 8192, "z": W.Z95, "bytes": 2 * gelu_bytes(64, 8192)},
+        {"op": "gelu_native", "T": 2048, "d": 16384, "z": W.Z95,
+         "bytes": gelu_bytes(2048, 16384)},
+        {"op": "gelu_native", "T": 64, "d": 8192, "z": W.Z95, "bytes": gelu_bytes(64, 8192)},
     ]
 
 
@@ -285,6 +289,8 @@ def _launch(ga, L, x, out):
         ga.squared_relu(x, out=out)
     elif op in ("gelu_f16", "gelu_f32"):
         ga.gelu_and_mul_sparse(x, L["z"], d=L["d"], out=out)
+    elif op == "gelu_native":
+        ga.gelu_and_mul_sparse_native(x, L["z"], d=L["d"], out=out)
     else:
         raise ValueError(op)
 
