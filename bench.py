@@ -117,12 +117,21 @@ def load_peaks() -> dict:
         return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "fallback"}
 
 
+def _code_only(text: str) -> str:
+    """Source text without comments and whitespace (the hash tracks code only)."""
+    import re
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return re.sub(r"\s+", "", text)
+
+
 def kernel_sources_hash() -> str:
+    """Hash of the library's CUDA/C++ code (comments and whitespace ignored)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "gated_activation_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+        with open(os.path.join(csrc, f)) as fh:
+            h.update(f.encode() + _code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

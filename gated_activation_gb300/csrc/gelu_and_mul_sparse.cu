@@ -2,8 +2,9 @@
 // pass over HBM.
 //
 // Definition (vLLM PR "[Performance] Add Triton kernel for Gemma3n sparse
-// GELU", section "Purpose": per-row mean and variance, Gaussian thresholding,
-// tanh GELU, gated multiplication), per row with gate g = [0, d), up u = [d, 2d):
+// GELU", section "Purpose", which lists the fused stages: row statistics, a
+// threshold derived from them, the tanh form of GELU and the product with the
+// up half), per row with gate g = [0, d), up u = [d, 2d):
 //   mean = sum g / d,  std = sqrt(sum (g - mean)^2 / d),  cutoff = mean + std z,
 //   out  = gelu_tanh(max(g - cutoff, 0)) * u,  fp32 math, one bf16 rounding.
 //

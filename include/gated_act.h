@@ -5,10 +5,10 @@
  * library is built around:
  *
  *   gelu_and_mul_sparse  Gemma3n's sparse GELU gate.  vLLM PR "[Performance]
- *       Add Triton kernel for Gemma3n sparse GELU", section "Purpose": per-row
- *       mean and variance, Gaussian thresholding, tanh GELU and the gated
- *       multiplication, fused.  For each row with gate g = columns [0, d) and
- *       up u = columns [d, 2d):
+ *       Add Triton kernel for Gemma3n sparse GELU", section "Purpose" (the
+ *       fused stages: row statistics, a threshold set from them, the tanh form
+ *       of GELU, the product with the up half).  For each row with gate
+ *       g = columns [0, d) and up u = columns [d, 2d):
  *           mean   = sum_j g_j / d                    (fp32 accumulation)
  *           std    = sqrt(sum_j (g_j - mean)^2 / d)   (population std)
  *           cutoff = mean + std * z,   z = inverse normal CDF of the target
@@ -251,9 +251,9 @@ int gelu_and_mul_sparse_typed(void *out, const void *in, int64_t T, int64_t d,
 /*
  * gelu_and_mul_sparse in native-rounding mode: the op computed as the
  * composition of separate element-type ops does it, every intermediate
- * rounded to the element type.  This is what the sparse-GELU page's kernel
- * does to reproduce native PyTorch ("Cross-architecture warp and dtype
- * validation": input-dtype roundtrips at operation boundaries).  Each op
+ * rounded to the element type -- what the sparse-GELU page's kernel does to
+ * match PyTorch's own sequence of ops ("Cross-architecture warp and dtype
+ * validation").  Each op
  * runs in fp32 and its result is rounded (nearest even) to the element type:
  *   m = R(mean g), sd = R(population std g), t = R(sd * z), c = R(m + t),
  *   s = relu(R(g - c)), a = R(gelu_tanh(s)), out = R(a * u).

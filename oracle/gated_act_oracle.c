@@ -9,10 +9,10 @@
  * loop per stage, with no blocking, fusion or reordering:
  *
  *  gelu_and_mul_sparse  -- vLLM PR "[Performance] Add Triton kernel for
- *      Gemma3n sparse GELU", section "Purpose": the activation takes per-row
- *      mean and variance, a Gaussian threshold, tanh GELU and the gated
- *      multiplication.  Reading of each stage (the page names the stages but
- *      prints no formula):
+ *      Gemma3n sparse GELU", section "Purpose": the activation fuses the row
+ *      statistics, a threshold set from them, the tanh form of GELU and the
+ *      product with the up half.  Reading of each stage (the page lists the
+ *      stages but prints no formula):
  *        gate g = columns [0, d) of the row, up u = columns [d, 2d);
  *        mean   = sum_j g_j / d;
  *        var    = sum_j (g_j - mean)^2 / d       (population variance);
@@ -265,9 +265,9 @@ double oracle_round_bf16(double v)
 
 /*
  * gelu_and_mul_sparse in native-rounding mode: the op as a composition of
- * separate element-type ops, as the sparse-GELU page's kernel reproduces
- * native PyTorch ("Cross-architecture warp and dtype validation":
- * input-dtype roundtrips at operation boundaries).  Each op of an element
+ * separate element-type ops, which the sparse-GELU page's kernel imitates
+ * ("Cross-architecture warp and dtype validation": it rounds intermediates
+ * back to the input type where PyTorch's separate ops would).  Each op of an element
  * type is computed in binary32 and its result rounded to the element type
  * (bf16 or fp16), so a boundary is R(x) = round_T(round_binary32(x)) with x
  * the op's exact value -- two roundings, which differ from one when the

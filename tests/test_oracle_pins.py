@@ -8,8 +8,8 @@ the oracle (a dropped term, a sign, sample instead of population variance,
 swapped gate/up halves, a double rounding) fails at least one of them.
 
 Definition pinned: vLLM PR "[Performance] Add Triton kernel for Gemma3n sparse
-GELU", section "Purpose" (per-row mean and variance, Gaussian thresholding,
-tanh GELU, gated multiplication), read as
+GELU", section "Purpose" (the fused stages: row statistics, a threshold from
+them, tanh GELU, the product with the up half), read as
     out = gelu_tanh(relu(gate - (mean + std * z))) * up,  std = population std;
 and Megatron-LM PR "Size MoE activation kernel grid to the row count",
 section "What changed and why" (out = silu(gate) * up).
