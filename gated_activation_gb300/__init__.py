@@ -32,7 +32,8 @@ EXPORTED = (
     "gelu_and_mul_sparse", "gelu_and_mul_sparse_typed", "gelu_and_mul_sparse_native",
     "silu_and_mul", "gated_act_status_string",
     "gated_act_last_cuda_error", "gelu_and_mul_sparse_plan", "gelu_and_mul_sparse_ex",
-    "gated_act_device_status", "gated_act_noop", "silu_and_mul_bounded", "gelu_and_mul",
+    "gated_act_device_status", "gated_act_noop", "gated_act_selftest_wait_timeout",
+    "silu_and_mul_bounded", "gelu_and_mul",
     "squared_relu",
 )
 
@@ -99,6 +100,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.gated_act_device_status.restype = ctypes.c_int
     lib.gated_act_noop.argtypes = [vp]
     lib.gated_act_noop.restype = ctypes.c_int
+    lib.gated_act_selftest_wait_timeout.argtypes = [vp, cvp, i64, i64, ctypes.c_ulonglong, vp]
+    lib.gated_act_selftest_wait_timeout.restype = ctypes.c_int
     lib.silu_and_mul_bounded.argtypes = [vp, cvp, i64, i64, cvp, vp]
     lib.silu_and_mul_bounded.restype = ctypes.c_int
     lib.gelu_and_mul.argtypes = [vp, cvp, i64, i64, i64, vp]

@@ -313,15 +313,15 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
-// Wait for the phase `parity` of `bar`, giving up after kWaitLimitNs.
-__device__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// Wait for the phase `parity` of `bar`, giving up after limit_ns.
+__device__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
     if (mbar_try_wait(bar, parity))
         return true;
     const unsigned long long t0 = globaltimer_ns();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity))
             return true;
-        if ((i & 255u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs)
+        if ((i & 255u) == 0 && globaltimer_ns() - t0 > limit_ns)
             return false;
     }
 }
@@ -334,10 +334,12 @@ __device__ bool mbar_wait(uint32_t bar, uint32_t parity) {
 // follows the slot's last read: at the first CTA barrier of row k, chunks up
 // to 2k are consumed (gate k is in registers, up k-1 was consumed by row
 // k-1's epilogue), so chunks up to 2k + S may be in flight.
+// withhold >= 0 (failure-handling tests only): every CTA skips issuing its
+// chunk number `withhold`, so the wait for it runs out after wait_ns.
 template <int NT, int V>
 __global__ void __launch_bounds__(NT, (1024 / NT) > 0 ? (1024 / NT) : 1)
 gelu_tma_rows(uint16_t *__restrict__ out, const uint16_t *__restrict__ in, int64_t T, int d,
-              int64_t rs, float z, int S) {
+              int64_t rs, float z, int S, int64_t withhold, unsigned long long wait_ns) {
     constexpr int NW = NT / 32;
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ float red[2][NW];
@@ -366,6 +368,8 @@ gelu_tma_rows(uint16_t *__restrict__ out, const uint16_t *__restrict__ in, int64
             return;
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         for (; issued < nchunks && issued <= last; ++issued) {
+            if (issued == withhold)
+                continue;
             const int64_t row = blockIdx.x + (issued >> 1) * G;
             const uint16_t *src = in + row * rs + ((issued & 1) ? d : 0);
             const uint32_t slot = static_cast<uint32_t>(issued % S);
@@ -381,7 +385,7 @@ gelu_tma_rows(uint16_t *__restrict__ out, const uint16_t *__restrict__ in, int64
         const int64_t row = blockIdx.x + k * G;
         const int64_t cg = 2 * k, cu = 2 * k + 1;
         const uint32_t sg = static_cast<uint32_t>(cg % S), su = static_cast<uint32_t>(cu % S);
-        bad |= !mbar_wait(bars + 8u * sg, static_cast<uint32_t>((cg / S) & 1));
+        bad |= !mbar_wait(bars + 8u * sg, static_cast<uint32_t>((cg / S) & 1), wait_ns);
 
         const uint4 *gs = reinterpret_cast<const uint4 *>(smem + static_cast<size_t>(sg) * chunk);
         uint4 g[V];
@@ -413,7 +417,7 @@ gelu_tma_rows(uint16_t *__restrict__ out, const uint16_t *__restrict__ in, int64
         const float sd = __fsqrt_rn(__fdiv_rn(q, static_cast<float>(d)));
         const float cutoff = fmaf(sd, z, mean);
 
-        bad |= !mbar_wait(bars + 8u * su, static_cast<uint32_t>((cu / S) & 1));
+        bad |= !mbar_wait(bars + 8u * su, static_cast<uint32_t>((cu / S) & 1), wait_ns);
         if (!bad) {
             const uint4 *us = reinterpret_cast<const uint4 *>(smem + static_cast<size_t>(su) * chunk);
             uint16_t *op = out + row * static_cast<int64_t>(d);
@@ -433,7 +437,7 @@ gelu_tma_rows(uint16_t *__restrict__ out, const uint16_t *__restrict__ in, int64
         atomicOr(&g_device_status, 1u);
         for (int64_t c = k > 0 ? 2 * k - 1 : 0; c < issued; ++c)
             mbar_wait(bars + 8u * static_cast<uint32_t>(c % S),
-                      static_cast<uint32_t>((c / S) & 1));
+                      static_cast<uint32_t>((c / S) & 1), wait_ns);
     }
 }
 
@@ -656,7 +660,8 @@ gelu_scalar_rows(void *__restrict__ out_, const void *__restrict__ in_, int64_t 
 using WarpFn = void (*)(uint16_t *, const uint16_t *, int64_t, int, int64_t, float);
 using CtaFn = void (*)(void *, const void *, int64_t, int, int64_t, float, int, int);
 using ScalarFn = void (*)(void *, const void *, int64_t, int64_t, int64_t, float);
-using TmaFn = void (*)(uint16_t *, const uint16_t *, int64_t, int, int64_t, float, int);
+using TmaFn = void (*)(uint16_t *, const uint16_t *, int64_t, int, int64_t, float, int, int64_t,
+                      unsigned long long);
 
 WarpFn warp_fn(int v) {
     switch (v) {
@@ -965,7 +970,8 @@ int ensure_smem_attr(TmaFn fn, int nt) {
 }
 
 int launch(const Plan &p, void *out, const void *in, int64_t T, int64_t d, int64_t rs,
-           double z, cudaStream_t stream) {
+           double z, cudaStream_t stream, int64_t withhold = -1,
+           unsigned long long wait_ns = kWaitLimitNs) {
     uint16_t *o = static_cast<uint16_t *>(out);
     const uint16_t *x = static_cast<const uint16_t *>(in);
     const float zf = static_cast<float>(z);
@@ -982,7 +988,7 @@ int launch(const Plan &p, void *out, const void *in, int64_t T, int64_t d, int64
         if (rc != GATED_ACT_OK)
             return rc;
         e = launch_kernel(fn, grid, block, static_cast<size_t>(q.smem_bytes), stream, 1, o, x, T,
-                          di, rs, zf, static_cast<int>(q.stages));
+                          di, rs, zf, static_cast<int>(q.stages), withhold, wait_ns);
         break;
     }
     case GATED_ACT_VARIANT_WARP_ROWS:
@@ -1056,6 +1062,19 @@ extern "C" int gelu_and_mul_sparse(void *out, const void *in, int64_t T, int64_t
                                    int64_t row_stride, double z, cudaStream_t stream) {
     return gelu_and_mul_sparse_typed(out, in, T, d, row_stride, z, GATED_ACT_BF16,
                                      GATED_ACT_VARIANT_AUTO, 0, stream);
+}
+
+extern "C" int gated_act_selftest_wait_timeout(void *out, const void *in, int64_t T, int64_t d,
+                                              unsigned long long wait_ns, cudaStream_t stream) {
+    if (wait_ns == 0 || wait_ns > gact::kWaitLimitNs)
+        return GATED_ACT_ERR_SIZE;
+    gact::Plan p;
+    const int rc = gact::make_plan(out, in, T, d, 2 * d, GATED_ACT_BF16,
+                                   GATED_ACT_VARIANT_TMA_ROWS, 0, 0, true, &p);
+    if (rc != GATED_ACT_OK || T == 0)
+        return rc;
+    // chunk 1 is the up half of each CTA's first row
+    return gact::launch(p, out, in, T, d, 2 * d, 1.0, stream, 1, wait_ns);
 }
 
 extern "C" int gated_act_device_status(unsigned int *flags) {

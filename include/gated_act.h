@@ -166,6 +166,21 @@ int gated_act_last_cuda_error(void);
  */
 int gated_act_device_status(unsigned int *flags);
 
+/*
+ * Exercise the bounded-wait give-up path of the TMA-rows kernel (for tests of
+ * the failure handling).  Runs gelu_and_mul_sparse on contiguous [T, 2d] bf16
+ * rows with the TMA-rows geometry, except that every CTA withholds the bulk
+ * copy of its first row's up half, so the wait for it runs out after wait_ns
+ * (0 < wait_ns <= 1e9).  Each CTA then records bit 0 of the device status,
+ * waits (bounded) for the copies it did issue and exits: no copy is left in
+ * flight and the context stays usable.  Rows a CTA did not finish are left
+ * unwritten.  Needs the 16-byte layout and d <= 32768
+ * (GATED_ACT_ERR_VARIANT otherwise).
+ */
+int gated_act_selftest_wait_timeout(void *out, const void *in, int64_t T,
+                                    int64_t d, unsigned long long wait_ns,
+                                    cudaStream_t stream);
+
 /* ------------------------------------------------------------------------
  * Launch-geometry control, for tests and measurements.
  *

@@ -1,0 +1,48 @@
+"""Failure handling of the bounded waits, on the GPU without a fault: every
+CTA of a TMA-rows launch withholds one bulk copy, so its wait runs out after
+a short limit.  The kernel must record the status bit, drain its own copies
+and return; the context must stay usable and later calls correct."""
+import ctypes
+
+import pytest
+import torch
+
+import workloads as W
+from tests.gpu_util import require_gpu
+from tests.parity import check_gelu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ga():
+    return require_gpu()
+
+
+def test_wait_runs_out_and_is_reported(ga, oracle):
+    assert ga.device_status() == 0
+    inp = W.iid(400, 4096, seed=11)
+    x = inp.x.cuda()
+    out = torch.zeros((400, 4096), dtype=torch.bfloat16, device="cuda")
+    lib = ga.load_library()
+    rc = lib.gated_act_selftest_wait_timeout(out.data_ptr(), x.data_ptr(), 400, 4096,
+                                             20_000_000, torch.cuda.current_stream().cuda_stream)
+    assert rc == 0
+    torch.cuda.synchronize()              # the launch ends: every wait was bounded
+    assert ga.device_status() == 1        # bit 0: a wait gave up
+    assert ga.device_status() == 0        # reading clears it
+    # the context is usable and the same kernel is correct without the fault
+    res = oracle.gelu_and_mul_sparse(W.to_bits(inp.x), d=4096, z=inp.z)
+    good = ga.gelu_and_mul_sparse(x, inp.z, variant=ga.VARIANT_TMA_ROWS)
+    torch.cuda.synchronize()
+    check_gelu(good.cpu(), inp.x, 4096, res, "after timeout")
+    assert ga.device_status() == 0
+
+
+def test_selftest_rejects_unbounded_limits(ga):
+    lib = ga.load_library()
+    x = torch.zeros((4, 64), dtype=torch.bfloat16, device="cuda")
+    o = torch.zeros((4, 32), dtype=torch.bfloat16, device="cuda")
+    assert lib.gated_act_selftest_wait_timeout(o.data_ptr(), x.data_ptr(), 4, 32, 0, None) == ga.ERR_SIZE
+    assert lib.gated_act_selftest_wait_timeout(o.data_ptr(), x.data_ptr(), 4, 32, 2_000_000_000,
+                                               None) == ga.ERR_SIZE
