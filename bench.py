@@ -497,6 +497,12 @@ def run_ours(args, world, rank, local):
                 "traffic": None if traffic is None else round(traffic)}
 
     e2e = run_e2e(args, launches, host_in, world, local, dev)
+    e2e_direct = run_e2e_host_direct(args, launches, host_in, world, local, dev)
+    link = link_ceiling(e2e["h2d_bytes_per_step"], e2e["d2h_bytes_per_step"], dev)
+    for rec in (e2e, e2e_direct):
+        rec["link_ceiling"] = link["value"]
+        rec["frac_of_link"] = round(rec["value"] / world / link["value"], 4)
+    e2e["link"] = link
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -518,7 +524,8 @@ def run_ours(args, world, rank, local):
                                  "graph B (the rest), CUDA events between the two replays",
                        "parallelism": f"rows sharded over {world} GPU(s), no collective",
                        "launch_floor_us": None if floor_us is None else round(floor_us, 3)},
-            "roofline": roofline, "e2e": e2e, "gpu_launches": len(launches) * args.steps,
+            "roofline": roofline, "e2e": e2e, "e2e_host_direct": e2e_direct,
+            "gpu_launches": len(launches) * args.steps,
             "clocks": clk.summary(), "per_shape": shapes_step, "widened_rows": widened}
     if cpu is not None:
         line["cpu_baseline"] = cpu
@@ -590,6 +597,96 @@ def run_e2e(args, launches, host_in, world, local, dev) -> dict:
             "ms_per_step": round(ms, 4), "steps": steps,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "pipeline": "3 streams: H2D / kernels / D2H, pinned host buffers"}
+
+
+def link_ceiling(h2d: int, d2h: int, dev) -> dict:
+    """What the CPU-GPU link itself carries for this step's mix of directions:
+    copy-engine copies between page-locked host and device buffers, H2D and D2H
+    at once on two streams in the step's byte ratio, plus each direction alone.
+    The end-to-end figures above cannot beat the first number."""
+    import torch
+    unit = 256 << 20
+    n_in = unit
+    n_out = max(16, int(unit * d2h / max(h2d, 1)) // 16 * 16)
+    hi = torch.empty(n_in, dtype=torch.uint8).pin_memory()
+    ho = torch.empty(n_out, dtype=torch.uint8).pin_memory()
+    di = torch.empty(n_in, dtype=torch.uint8, device=dev)
+    do = torch.empty(n_out, dtype=torch.uint8, device=dev)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def timed(fn, reps=5):
+        fn()
+        torch.cuda.synchronize()
+        cur = torch.cuda.current_stream()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(cur)
+        for s in (s1, s2):
+            s.wait_event(a)
+        for _ in range(reps):
+            fn()
+        for s in (s1, s2):
+            cur.wait_stream(s)
+        b.record(cur)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) * 1e-3 / reps
+
+    def up():
+        with torch.cuda.stream(s1):
+            di.copy_(hi, non_blocking=True)
+
+    def down():
+        with torch.cuda.stream(s2):
+            ho.copy_(do, non_blocking=True)
+
+    def both():
+        up()
+        down()
+
+    t_both, t_up, t_down = timed(both), timed(up), timed(down)
+    return {"value": round((n_in + n_out) / t_both / 1e9, 1), "unit": "GB/s",
+            "h2d_alone": round(n_in / t_up / 1e9, 1), "d2h_alone": round(n_out / t_down / 1e9, 1),
+            "mix_h2d_to_d2h": round(h2d / max(d2h, 1), 3),
+            "method": "cudaMemcpyAsync between page-locked host and device buffers, "
+                      "both directions at once in the step's byte ratio"}
+
+
+def run_e2e_host_direct(args, launches, host_in, world, local, dev) -> dict:
+    """The same public calls given page-locked HOST buffers directly: the
+    kernels read each input and write each output over the CPU-GPU link in
+    place, so no copy is issued.  The bytes crossing the link per step equal
+    the explicit-copy path's."""
+    import torch
+    import gated_activation_gb300 as ga
+    pin_in = {k: v.pin_memory() for k, v in host_in.items()}
+    pin_out = [torch.empty((L["T"], L["d"]), dtype=torch.bfloat16).pin_memory() for L in launches]
+    h2d = sum(host_in[L["key"]].numel() * 2 for L in launches)
+    d2h = sum(L["T"] * L["d"] * 2 for L in launches)
+
+    def step():
+        for i, L in enumerate(launches):
+            _launch(ga, L, pin_in[L["key"]], pin_out[i])
+
+    steps = max(1, min(args.steps, args.e2e_steps))
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    barrier(world, local)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        step()
+    b.record()
+    torch.cuda.synchronize()
+    barrier(world, local)
+    ms = max_over_ranks(a.elapsed_time(b) / steps, world, dev)
+    bytes_step = sum(L["bytes"] for L in launches)
+    return {"value": round(world * bytes_step / (ms * 1e-3) / 1e9, 1), "unit": UNIT,
+            "ms_per_step": round(ms, 4), "steps": steps,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "transfer": "kernels read the inputs from and write the results to page-locked "
+                        "host buffers in place (NVLink-C2C); no copy is issued"}
 
 
 # ----------------------------------------------------------------- the oracle on host cores

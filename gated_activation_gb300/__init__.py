@@ -1,9 +1,10 @@
 """Python binding of the GB300 fused gated-activation library.
 
-Argument marshalling only: every step of both activations runs in the CUDA
+Argument marshalling only: every step of the activations runs in the CUDA
 library ``_lib/libgated_act.so`` (built from ``csrc/`` by ``build.py``) behind
-the C ABI declared in ``include/gated_act.h``.  PyTorch supplies device memory
-and the current stream.  There is no CPU or eager fallback: if the library is
+the C ABI declared in ``include/gated_act.h``.  PyTorch supplies memory
+(device, or page-locked host memory the kernels read and write in place) and
+the current stream.  There is no CPU or eager fallback: if the library is
 missing or a call fails, this module raises.
 """
 from __future__ import annotations
@@ -20,7 +21,7 @@ LIB_PATH = _build.LIB
 
 OK = 0
 ERR_NULL, ERR_SIZE, ERR_STRIDE, ERR_TOO_LARGE = -1, -2, -3, -4
-ERR_OVERLAP, ERR_VARIANT, ERR_CUDA, ERR_ALIGN, ERR_DTYPE = -5, -6, -7, -8, -9
+ERR_OVERLAP, ERR_VARIANT, ERR_CUDA, ERR_ALIGN, ERR_DTYPE, ERR_HOST = -5, -6, -7, -8, -9, -10
 
 BF16, F16, F32 = 0, 1, 2
 _DTYPE_CODE = {torch.bfloat16: BF16, torch.float16: F16, torch.float32: F32}
@@ -125,19 +126,31 @@ def _check(fn: str, rc: int) -> None:
         raise GatedActError(fn, rc, msg)
 
 
+def _empty_like_rows(x: torch.Tensor, T: int, d: int) -> torch.Tensor:
+    """An output [T, d] of x's type where x lives: device, or page-locked host."""
+    if x.is_cuda:
+        return torch.empty((T, d), dtype=x.dtype, device=x.device)
+    return torch.empty((T, d), dtype=x.dtype, pin_memory=True)
+
+
+def _is_device_or_pinned(x: torch.Tensor) -> bool:
+    return x.is_cuda or x.is_pinned()
+
+
 def _stream_handle(stream: torch.cuda.Stream | None) -> int:
     s = stream if stream is not None else torch.cuda.current_stream()
     return int(s.cuda_stream)
 
 
 def _rows_view(x: torch.Tensor, dtypes=(torch.bfloat16,)) -> tuple[int, int]:
-    """(T, row_stride) for a 2-D CUDA tensor whose rows may be strided."""
+    """(T, row_stride) for a 2-D device or page-locked tensor whose rows may be strided."""
     if x.dim() != 2:
         raise ValueError("input must be 2-D [T, row_stride]")
     if x.dtype not in dtypes:
         raise TypeError(f"input must be one of {dtypes}")
-    if not x.is_cuda:
-        raise ValueError("input must be a CUDA tensor (the library has no CPU path)")
+    if not (x.is_cuda or x.is_pinned()):
+        raise ValueError("input must be a CUDA tensor or page-locked host memory "
+                         "(the library has no CPU path)")
     if x.stride(1) != 1:
         raise ValueError("input columns must be contiguous")
     return int(x.shape[0]), int(x.stride(0)) if x.shape[0] > 1 else int(x.shape[1])
@@ -146,8 +159,8 @@ def _rows_view(x: torch.Tensor, dtypes=(torch.bfloat16,)) -> tuple[int, int]:
 def gelu_and_mul_sparse(x: torch.Tensor, z: float, d: int | None = None,
                         out: torch.Tensor | None = None, variant: int = VARIANT_AUTO,
                         cluster: int = 0, stream: torch.cuda.Stream | None = None) -> torch.Tensor:
-    """Sparse GELU gate of ``x`` ([T, >=2d] bf16, fp16 or fp32 CUDA): returns
-    ``out`` [T, d] of the same type.
+    """Sparse GELU gate of ``x`` ([T, >=2d] bf16, fp16 or fp32, on the device or
+    in page-locked host memory): returns ``out`` [T, d] of the same type.
 
     ``d`` defaults to half the row length.  Rows may be strided (x[:, :2d] of a
     wider buffer).  ``variant``/``cluster`` force a launch geometry.
@@ -160,7 +173,7 @@ def gelu_and_mul_sparse(x: torch.Tensor, z: float, d: int | None = None,
     if x.shape[1] < 2 * d:
         raise ValueError("rows are shorter than 2d")
     if out is None:
-        out = torch.empty((T, d), dtype=x.dtype, device=x.device)
+        out = _empty_like_rows(x, T, d)
     elif out.shape != (T, d) or out.dtype != x.dtype or not out.is_contiguous():
         raise ValueError(f"out must be a contiguous [T, d] {x.dtype} tensor")
     lib = load_library()
@@ -174,7 +187,7 @@ def gelu_and_mul_sparse(x: torch.Tensor, z: float, d: int | None = None,
 def gelu_and_mul_sparse_native(x: torch.Tensor, z: float, d: int | None = None,
                                out: torch.Tensor | None = None,
                                stream: torch.cuda.Stream | None = None) -> torch.Tensor:
-    """Native-rounding sparse GELU of ``x`` ([T, >=2d] bf16 or fp16 CUDA): every
+    """Native-rounding sparse GELU of ``x`` ([T, >=2d] bf16 or fp16): every
     intermediate rounded to the element type, as separate PyTorch ops round."""
     T, rs = _rows_view(x, (torch.bfloat16, torch.float16))
     if d is None:
@@ -184,7 +197,7 @@ def gelu_and_mul_sparse_native(x: torch.Tensor, z: float, d: int | None = None,
     if x.shape[1] < 2 * d:
         raise ValueError("rows are shorter than 2d")
     if out is None:
-        out = torch.empty((T, d), dtype=x.dtype, device=x.device)
+        out = _empty_like_rows(x, T, d)
     elif out.shape != (T, d) or out.dtype != x.dtype or not out.is_contiguous():
         raise ValueError(f"out must be a contiguous [T, d] {x.dtype} tensor")
     rc = load_library().gelu_and_mul_sparse_native(out.data_ptr(), x.data_ptr(), T, d, rs,
@@ -225,15 +238,18 @@ def noop(stream: torch.cuda.Stream | None = None) -> None:
 
 def silu_and_mul(x: torch.Tensor, out: torch.Tensor | None = None,
                  stream: torch.cuda.Stream | None = None) -> torch.Tensor:
-    """silu(gate) * up of a contiguous [M, 2d] bf16 CUDA tensor: returns [M, d] bf16."""
-    if x.dim() != 2 or x.dtype != torch.bfloat16 or not x.is_cuda or not x.is_contiguous():
-        raise ValueError("input must be a contiguous 2-D bf16 CUDA tensor [M, 2d]")
+    """silu(gate) * up of a contiguous [M, 2d] bf16 tensor (CUDA or page-locked
+    host): returns [M, d] bf16 where x lives."""
+    if x.dim() != 2 or x.dtype != torch.bfloat16 or not _is_device_or_pinned(x) \
+            or not x.is_contiguous():
+        raise ValueError("input must be a contiguous 2-D bf16 tensor [M, 2d] on the device "
+                         "or in page-locked host memory")
     M, w = int(x.shape[0]), int(x.shape[1])
     if w % 2:
         raise ValueError("row length must be even (2d)")
     d = w // 2
     if out is None:
-        out = torch.empty((M, d), dtype=torch.bfloat16, device=x.device)
+        out = _empty_like_rows(x, M, d)
     elif out.shape != (M, d) or out.dtype != torch.bfloat16 or not out.is_contiguous():
         raise ValueError("out must be a contiguous [M, d] bf16 tensor")
     rc = load_library().silu_and_mul(out.data_ptr(), x.data_ptr(), M, d, _stream_handle(stream))
@@ -252,9 +268,9 @@ def _gated_in(x: torch.Tensor, d: int | None) -> tuple[int, int, int]:
     return T, rs, d
 
 
-def _out_for(out: torch.Tensor | None, T: int, d: int, device) -> torch.Tensor:
+def _out_for(out: torch.Tensor | None, T: int, d: int, like: torch.Tensor) -> torch.Tensor:
     if out is None:
-        return torch.empty((T, d), dtype=torch.bfloat16, device=device)
+        return _empty_like_rows(like, T, d)
     if out.shape != (T, d) or out.dtype != torch.bfloat16 or not out.is_contiguous():
         raise ValueError(f"out must be a contiguous [{T}, {d}] bf16 tensor")
     return out
@@ -262,16 +278,17 @@ def _out_for(out: torch.Tensor | None, T: int, d: int, device) -> torch.Tensor:
 
 def silu_and_mul_bounded(x: torch.Tensor, n_rows: torch.Tensor, out: torch.Tensor | None = None,
                          stream: torch.cuda.Stream | None = None) -> torch.Tensor:
-    """silu_and_mul over the first ``n_rows`` rows (a 1-element int32 CUDA tensor).
+    """silu_and_mul over the first ``n_rows`` rows (a 1-element int32 tensor).
 
     Rows at or past the live count are left untouched in ``out``.
     """
-    if x.dim() != 2 or x.dtype != torch.bfloat16 or not x.is_cuda or not x.is_contiguous():
-        raise ValueError("input must be a contiguous 2-D bf16 CUDA tensor [M, 2d]")
-    if n_rows.dtype != torch.int32 or not n_rows.is_cuda or n_rows.numel() < 1:
-        raise ValueError("n_rows must be an int32 CUDA tensor")
+    if x.dim() != 2 or x.dtype != torch.bfloat16 or not _is_device_or_pinned(x) \
+            or not x.is_contiguous():
+        raise ValueError("input must be a contiguous 2-D bf16 tensor [M, 2d]")
+    if n_rows.dtype != torch.int32 or not _is_device_or_pinned(n_rows) or n_rows.numel() < 1:
+        raise ValueError("n_rows must be an int32 tensor on the device or in page-locked memory")
     M, d = int(x.shape[0]), int(x.shape[1]) // 2
-    out = _out_for(out, M, d, x.device)
+    out = _out_for(out, M, d, x)
     rc = load_library().silu_and_mul_bounded(out.data_ptr(), x.data_ptr(), M, d,
                                              n_rows.data_ptr(), _stream_handle(stream))
     _check("silu_and_mul_bounded", rc)
@@ -280,9 +297,9 @@ def silu_and_mul_bounded(x: torch.Tensor, n_rows: torch.Tensor, out: torch.Tenso
 
 def gelu_and_mul(x: torch.Tensor, d: int | None = None, out: torch.Tensor | None = None,
                  stream: torch.cuda.Stream | None = None) -> torch.Tensor:
-    """Dense gelu_tanh(gate) * up of ``x`` ([T, >=2d] bf16 CUDA): returns [T, d] bf16."""
+    """Dense gelu_tanh(gate) * up of ``x`` ([T, >=2d] bf16): returns [T, d] bf16."""
     T, rs, d = _gated_in(x, d)
-    out = _out_for(out, T, d, x.device)
+    out = _out_for(out, T, d, x)
     rc = load_library().gelu_and_mul(out.data_ptr(), x.data_ptr(), T, d, rs, _stream_handle(stream))
     _check("gelu_and_mul", rc)
     return out
@@ -290,11 +307,12 @@ def gelu_and_mul(x: torch.Tensor, d: int | None = None, out: torch.Tensor | None
 
 def squared_relu(x: torch.Tensor, out: torch.Tensor | None = None,
                  stream: torch.cuda.Stream | None = None) -> torch.Tensor:
-    """max(x, 0)^2 of a contiguous [M, d] bf16 CUDA tensor."""
-    if x.dim() != 2 or x.dtype != torch.bfloat16 or not x.is_cuda or not x.is_contiguous():
-        raise ValueError("input must be a contiguous 2-D bf16 CUDA tensor [M, d]")
+    """max(x, 0)^2 of a contiguous [M, d] bf16 tensor."""
+    if x.dim() != 2 or x.dtype != torch.bfloat16 or not _is_device_or_pinned(x) \
+            or not x.is_contiguous():
+        raise ValueError("input must be a contiguous 2-D bf16 tensor [M, d]")
     M, d = int(x.shape[0]), int(x.shape[1])
-    out = _out_for(out, M, d, x.device)
+    out = _out_for(out, M, d, x)
     rc = load_library().squared_relu(out.data_ptr(), x.data_ptr(), M, d, _stream_handle(stream))
     _check("squared_relu", rc)
     return out

@@ -39,6 +39,32 @@ bool pdl_enabled() {
     return on;
 }
 
+int resolve_ptr(const void *p, const void **dev, bool *host) {
+    *dev = p;
+    *host = false;
+    if (!p)
+        return GATED_ACT_OK;
+    cudaPointerAttributes a;
+    const cudaError_t e = cudaPointerGetAttributes(&a, p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();   // not sticky, but keep the error state clean
+        return GATED_ACT_ERR_HOST;
+    }
+    switch (a.type) {
+    case cudaMemoryTypeDevice:
+    case cudaMemoryTypeManaged:
+        return GATED_ACT_OK;
+    case cudaMemoryTypeHost:
+        if (!a.devicePointer)
+            return GATED_ACT_ERR_HOST;
+        *dev = a.devicePointer;
+        *host = true;
+        return GATED_ACT_OK;
+    default:   // not registered with CUDA: pageable host memory, or no allocation at all
+        return GATED_ACT_ERR_HOST;
+    }
+}
+
 int cuda_status(cudaError_t e) {
     if (e == cudaSuccess)
         return GATED_ACT_OK;
@@ -71,7 +97,9 @@ extern "C" const char *gated_act_status_string(int status) {
     case GATED_ACT_ERR_OVERLAP: return "output overlaps the input";
     case GATED_ACT_ERR_VARIANT: return "requested launch geometry does not fit this call";
     case GATED_ACT_ERR_CUDA: return "CUDA runtime error at launch (see gated_act_last_cuda_error)";
-    case GATED_ACT_ERR_ALIGN: return "pointer is not 2-byte aligned";
+    case GATED_ACT_ERR_ALIGN: return "pointer is not aligned to its element size";
+    case GATED_ACT_ERR_DTYPE: return "unknown or unsupported element type";
+    case GATED_ACT_ERR_HOST: return "memory the CUDA runtime does not know (pageable or unallocated)";
     default: return "unknown status";
     }
 }

@@ -112,6 +112,12 @@ cudaError_t launch_kernel(void (*kernel)(Exp...), dim3 grid, dim3 block, size_t 
 // Record a CUDA error for gated_act_last_cuda_error() and map it to a status.
 int cuda_status(cudaError_t e);
 
+// The address kernels use for `p`: device (and managed) memory as is;
+// page-locked host memory through its device mapping.  Sets *host when the
+// bytes live in host memory.  Returns GATED_ACT_OK, or GATED_ACT_ERR_HOST for
+// an address the runtime does not know (pageable memory, no allocation).
+int resolve_ptr(const void *p, const void **dev, bool *host);
+
 inline bool aligned(const void *p, uintptr_t a) {
     return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
 }

@@ -207,9 +207,17 @@ int run(void *out, const void *in, int64_t M, int64_t d, int64_t in_rs, const in
     if (ranges_overlap(out, out_bytes, in, in_bytes))
         return GATED_ACT_ERR_OVERLAP;
 
-    uint16_t *o = static_cast<uint16_t *>(out);
-    const uint16_t *x = static_cast<const uint16_t *>(in);
-    const bool vec_ok = aligned(in, 16) && aligned(out, 16) && d % 8 == 0 && in_rs % 8 == 0;
+    const void *dout, *din, *dn = n_rows;
+    bool host = false;
+    int rc;
+    if ((rc = resolve_ptr(out, &dout, &host)) != GATED_ACT_OK ||
+        (rc = resolve_ptr(in, &din, &host)) != GATED_ACT_OK ||
+        (BOUNDED && (rc = resolve_ptr(n_rows, &dn, &host)) != GATED_ACT_OK))
+        return rc;
+    n_rows = static_cast<const int32_t *>(dn);
+    uint16_t *o = static_cast<uint16_t *>(const_cast<void *>(dout));
+    const uint16_t *x = static_cast<const uint16_t *>(din);
+    const bool vec_ok = aligned(x, 16) && aligned(o, 16) && d % 8 == 0 && in_rs % 8 == 0;
     cudaError_t e;
     if (vec_ok) {
         const int64_t nv = d / 8;

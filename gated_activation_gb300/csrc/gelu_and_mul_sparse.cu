@@ -828,9 +828,10 @@ int validate(const void *out, const void *in, int64_t T, int64_t d, int64_t rs, 
     return GATED_ACT_OK;
 }
 
+// host_mem: in or out lives in host memory; only register-load kernels run.
 int make_plan(const void *out, const void *in, int64_t T, int64_t d, int64_t rs, int dtype,
               int variant, int cluster, int sm_count, bool check_ptrs, Plan *p,
-              bool native = false) {
+              bool native = false, bool host_mem = false) {
     if (dtype < GATED_ACT_BF16 || dtype > GATED_ACT_F32 || (native && dtype == GATED_ACT_F32))
         return GATED_ACT_ERR_DTYPE;
     const int elem = elem_bytes(dtype), epv = 16 / elem;
@@ -839,10 +840,13 @@ int make_plan(const void *out, const void *in, int64_t T, int64_t d, int64_t rs,
         return rc;
     if (variant < GATED_ACT_VARIANT_AUTO || variant > GATED_ACT_VARIANT_TMA_ROWS)
         return GATED_ACT_ERR_VARIANT;
-    // the warp-rows and TMA-rows kernels exist for plain bf16 only
+    // the warp-rows and TMA-rows kernels exist for plain bf16 only; bulk copies
+    // from host memory are not used
     const bool cta_only = dtype != GATED_ACT_BF16 || native;
     if (cta_only &&
         (variant == GATED_ACT_VARIANT_WARP_ROWS || variant == GATED_ACT_VARIANT_TMA_ROWS))
+        return GATED_ACT_ERR_VARIANT;
+    if (host_mem && variant == GATED_ACT_VARIANT_TMA_ROWS)
         return GATED_ACT_ERR_VARIANT;
     gated_act_plan &q = p->pub;
     q = gated_act_plan{};
@@ -855,7 +859,7 @@ int make_plan(const void *out, const void *in, int64_t T, int64_t d, int64_t rs,
     int t_cps = 0, t_nt = 0, t_stages = 0;
     int64_t t_smem = 0;
     const int want_cps = variant == GATED_ACT_VARIANT_TMA_ROWS ? cluster : 0;
-    const bool tma_ok = vec_ok && !cta_only &&
+    const bool tma_ok = vec_ok && !cta_only && !host_mem &&
                         tma_shape(nvec, want_cps, &t_cps, &t_nt, &t_stages, &t_smem);
 
     // Measured on GB300 (every geometry timed per T x d, graph-replayed over
@@ -1020,35 +1024,60 @@ extern "C" int gelu_and_mul_sparse_plan(const void *out, const void *in, int64_t
                                         int sm_count, gated_act_plan *plan) {
     if (!plan)
         return GATED_ACT_ERR_NULL;
+    // A buffer in page-locked host memory rules out the bulk-copy geometry, as
+    // at launch; a pointer the runtime cannot classify (no device, or not yet
+    // allocated) plans as device memory.
+    bool host = false;
+    for (const void *q : {out, in}) {
+        const void *dq;
+        bool h = false;
+        if (q && gact::resolve_ptr(q, &dq, &h) == GATED_ACT_OK)
+            host = host || h;
+    }
     gact::Plan p;
     const int rc = gact::make_plan(out, in, T, d, row_stride, dtype, variant, cluster, sm_count,
-                                   false, &p);
+                                   false, &p, false, host);
     if (rc != GATED_ACT_OK)
         return rc;
     *plan = p.pub;
     return GATED_ACT_OK;
 }
 
+namespace gact {
+namespace {
+// Validate, resolve host buffers, plan and launch one gelu_and_mul_sparse call.
+int run_gelu(void *out, const void *in, int64_t T, int64_t d, int64_t rs, double z, int dtype,
+             int variant, int cluster, bool native, cudaStream_t stream) {
+    Plan p;
+    int rc = make_plan(out, in, T, d, rs, dtype, variant, cluster, 0, true, &p, native);
+    if (rc != GATED_ACT_OK || T == 0)
+        return rc;
+    const void *dout, *din;
+    bool hout, hin;
+    if ((rc = resolve_ptr(out, &dout, &hout)) != GATED_ACT_OK ||
+        (rc = resolve_ptr(in, &din, &hin)) != GATED_ACT_OK)
+        return rc;
+    if (hout || hin) {
+        rc = make_plan(dout, din, T, d, rs, dtype, variant, cluster, 0, true, &p, native, true);
+        if (rc != GATED_ACT_OK)
+            return rc;
+    }
+    return launch(p, const_cast<void *>(dout), din, T, d, rs, z, stream);
+}
+}  // namespace
+}  // namespace gact
+
 extern "C" int gelu_and_mul_sparse_typed(void *out, const void *in, int64_t T, int64_t d,
                                          int64_t row_stride, double z, int dtype, int variant,
                                          int cluster, cudaStream_t stream) {
-    gact::Plan p;
-    const int rc =
-        gact::make_plan(out, in, T, d, row_stride, dtype, variant, cluster, 0, true, &p);
-    if (rc != GATED_ACT_OK || T == 0)
-        return rc;
-    return gact::launch(p, out, in, T, d, row_stride, z, stream);
+    return gact::run_gelu(out, in, T, d, row_stride, z, dtype, variant, cluster, false, stream);
 }
 
 extern "C" int gelu_and_mul_sparse_native(void *out, const void *in, int64_t T, int64_t d,
                                           int64_t row_stride, double z, int dtype,
                                           cudaStream_t stream) {
-    gact::Plan p;
-    const int rc = gact::make_plan(out, in, T, d, row_stride, dtype, GATED_ACT_VARIANT_AUTO, 0,
-                                   0, true, &p, true);
-    if (rc != GATED_ACT_OK || T == 0)
-        return rc;
-    return gact::launch(p, out, in, T, d, row_stride, z, stream);
+    return gact::run_gelu(out, in, T, d, row_stride, z, dtype, GATED_ACT_VARIANT_AUTO, 0, true,
+                          stream);
 }
 
 extern "C" int gelu_and_mul_sparse_ex(void *out, const void *in, int64_t T, int64_t d,

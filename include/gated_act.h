@@ -23,8 +23,14 @@
  *       bf16 out.
  *
  * Conventions shared by every entry point
- *   - bf16 means 2-byte IEEE bfloat16 storage; all pointers are DEVICE
- *     pointers of the current CUDA device, owned by the caller.  The library
+ *   - bf16 means 2-byte IEEE bfloat16 storage.  Pointers are owned by the
+ *     caller and address memory the current device can read and write:
+ *     device (or managed) memory, or page-locked host memory (cudaHostAlloc /
+ *     cudaHostRegister).  Host buffers are read and written by the kernels in
+ *     place, over the CPU-GPU link, with no separate copy (tma_rows is then
+ *     not used).  An address the CUDA runtime does not know -- pageable host
+ *     memory, or no allocation at all -- gives GATED_ACT_ERR_HOST with
+ *     nothing launched.  The library
  *     allocates nothing, keeps no state between calls, never synchronizes the
  *     host and launches only on `stream` (0 = the legacy default stream), so
  *     every call is asynchronous and can be captured in a CUDA graph.
@@ -61,7 +67,8 @@ typedef enum gated_act_status {
     GATED_ACT_ERR_VARIANT = -6,    /* a forced variant/cluster size does not fit the call */
     GATED_ACT_ERR_CUDA = -7,       /* the CUDA runtime reported an error at launch */
     GATED_ACT_ERR_ALIGN = -8,      /* a pointer is not aligned to its element size */
-    GATED_ACT_ERR_DTYPE = -9       /* unknown element type                        */
+    GATED_ACT_ERR_DTYPE = -9,      /* unknown element type                        */
+    GATED_ACT_ERR_HOST = -10       /* memory the CUDA runtime does not know       */
 } gated_act_status;
 
 /* Element types of the typed entry point (in and out share one type). */
