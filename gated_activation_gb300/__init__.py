@@ -35,7 +35,7 @@ EXPORTED = (
     "gated_act_last_cuda_error", "gelu_and_mul_sparse_plan", "gelu_and_mul_sparse_ex",
     "gated_act_device_status", "gated_act_noop", "gated_act_selftest_wait_timeout",
     "silu_and_mul_bounded", "gelu_and_mul",
-    "squared_relu",
+    "squared_relu", "gelu_and_mul_sparse_workspace_bytes", "gelu_and_mul_sparse_ws",
 )
 
 
@@ -51,14 +51,15 @@ class Plan(ctypes.Structure):
     _fields_ = [("variant", ctypes.c_int32), ("cluster", ctypes.c_int32),
                 ("threads", ctypes.c_int32), ("vec_per_thread", ctypes.c_int32),
                 ("rows_per_cta", ctypes.c_int32), ("stages", ctypes.c_int32),
-                ("ctas_per_sm", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("ctas_per_sm", ctypes.c_int32), ("dynamic_rows", ctypes.c_int32),
                 ("grid", ctypes.c_int64), ("smem_bytes", ctypes.c_int64)]
 
     def as_dict(self) -> dict:
         return {"variant": VARIANT_NAMES.get(self.variant, str(self.variant)),
                 "cluster": self.cluster, "threads": self.threads,
                 "vec_per_thread": self.vec_per_thread, "rows_per_cta": self.rows_per_cta,
-                "stages": self.stages, "ctas_per_sm": self.ctas_per_sm, "grid": self.grid,
+                "stages": self.stages, "ctas_per_sm": self.ctas_per_sm,
+                "dynamic_rows": self.dynamic_rows, "grid": self.grid,
                 "smem_bytes": self.smem_bytes}
 
 
@@ -109,6 +110,11 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.gelu_and_mul.restype = ctypes.c_int
     lib.squared_relu.argtypes = [vp, cvp, i64, i64, vp]
     lib.squared_relu.restype = ctypes.c_int
+    lib.gelu_and_mul_sparse_workspace_bytes.argtypes = []
+    lib.gelu_and_mul_sparse_workspace_bytes.restype = ctypes.c_size_t
+    lib.gelu_and_mul_sparse_ws.argtypes = [vp, cvp, i64, i64, i64, ctypes.c_double, ctypes.c_int,
+                                           ctypes.c_int, ctypes.c_int, vp, vp]
+    lib.gelu_and_mul_sparse_ws.restype = ctypes.c_int
     if path is None:
         _lib = lib
     return lib
@@ -156,14 +162,30 @@ def _rows_view(x: torch.Tensor, dtypes=(torch.bfloat16,)) -> tuple[int, int]:
     return int(x.shape[0]), int(x.stride(0)) if x.shape[0] > 1 else int(x.shape[1])
 
 
+def workspace_bytes() -> int:
+    """Bytes of the workspace ``gelu_and_mul_sparse(..., workspace=)`` takes."""
+    return int(load_library().gelu_and_mul_sparse_workspace_bytes())
+
+
+def new_workspace(device=None) -> torch.Tensor:
+    """A zeroed workspace on ``device``.  Calls that share it must run one after
+    another on the GPU (one stream, or ordered streams); every completed call
+    leaves it zeroed."""
+    return torch.zeros(workspace_bytes(), dtype=torch.uint8,
+                       device=device if device is not None else "cuda")
+
+
 def gelu_and_mul_sparse(x: torch.Tensor, z: float, d: int | None = None,
                         out: torch.Tensor | None = None, variant: int = VARIANT_AUTO,
-                        cluster: int = 0, stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+                        cluster: int = 0, stream: torch.cuda.Stream | None = None,
+                        workspace: torch.Tensor | None = None) -> torch.Tensor:
     """Sparse GELU gate of ``x`` ([T, >=2d] bf16, fp16 or fp32, on the device or
     in page-locked host memory): returns ``out`` [T, d] of the same type.
 
     ``d`` defaults to half the row length.  Rows may be strided (x[:, :2d] of a
     wider buffer).  ``variant``/``cluster`` force a launch geometry.
+    ``workspace`` (from :func:`new_workspace`) lets the persistent bulk-copy
+    geometry hand rows out dynamically; calls sharing one must not overlap.
     """
     T, rs = _rows_view(x, tuple(_DTYPE_CODE))
     if d is None:
@@ -177,10 +199,18 @@ def gelu_and_mul_sparse(x: torch.Tensor, z: float, d: int | None = None,
     elif out.shape != (T, d) or out.dtype != x.dtype or not out.is_contiguous():
         raise ValueError(f"out must be a contiguous [T, d] {x.dtype} tensor")
     lib = load_library()
-    rc = lib.gelu_and_mul_sparse_typed(out.data_ptr(), x.data_ptr(), T, d, rs, float(z),
-                                       _DTYPE_CODE[x.dtype], int(variant), int(cluster),
-                                       _stream_handle(stream))
-    _check("gelu_and_mul_sparse", rc)
+    if workspace is None:
+        rc = lib.gelu_and_mul_sparse_typed(out.data_ptr(), x.data_ptr(), T, d, rs, float(z),
+                                           _DTYPE_CODE[x.dtype], int(variant), int(cluster),
+                                           _stream_handle(stream))
+        _check("gelu_and_mul_sparse", rc)
+        return out
+    if not workspace.is_cuda or workspace.numel() * workspace.element_size() < workspace_bytes():
+        raise ValueError("workspace must be a device tensor of at least workspace_bytes() bytes")
+    rc = lib.gelu_and_mul_sparse_ws(out.data_ptr(), x.data_ptr(), T, d, rs, float(z),
+                                    _DTYPE_CODE[x.dtype], int(variant), int(cluster),
+                                    workspace.data_ptr(), _stream_handle(stream))
+    _check("gelu_and_mul_sparse_ws", rc)
     return out
 
 
@@ -320,4 +350,5 @@ def squared_relu(x: torch.Tensor, out: torch.Tensor | None = None,
 
 __all__ = ["gelu_and_mul_sparse_native", "silu_and_mul_bounded", "gelu_and_mul", "squared_relu", "gelu_and_mul_sparse", "gelu_and_mul_sparse_plan", "silu_and_mul", "device_status", "noop",
            "load_library",
-           "status_string", "GatedActError", "Plan", "EXPORTED", "LIB_PATH"]
+           "status_string", "GatedActError", "Plan", "EXPORTED", "LIB_PATH", "workspace_bytes",
+           "new_workspace"]

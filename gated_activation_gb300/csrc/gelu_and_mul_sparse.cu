@@ -52,6 +52,12 @@ constexpr int kTmaMaxStages = 8;
 constexpr int kTmaSmemPerSm = 228 * 1024;  // shared memory of one SM (1 KB per CTA is reserved)
 constexpr int kTmaSmemPerCta = 227 * 1024; // largest opt-in shared memory of one CTA
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;   // 1 s bound on every mbarrier wait
+// With a workspace, the bulk-copy geometry hands rows out dynamically from
+// this many rows per CTA on (measured on GB300: below it the static
+// round-robin is as fast, since a CTA takes its next row about one row ahead
+// of need and the last claims can then leave one CTA a row behind).
+constexpr int64_t kDynamicRowsPerCta = 6;
+constexpr size_t kWorkspaceBytes = 16;                       // two 64-bit counters
 
 // ------------------------------------------------------------ paired fp32 math
 __device__ __forceinline__ unsigned long long u64_of(float2 v) {
@@ -290,6 +296,10 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                  : "memory");
 }
+// An arrive with no transaction bytes: completes the phase of a count-1 barrier.
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
 // 1-D bulk copy global -> this CTA's shared memory, completing on `bar`.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
                                           uint32_t bar) {
@@ -327,30 +337,38 @@ __device__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned long long limi
 }
 
 // ------------------------------------------------------------ tma rows
-// Persistent CTA b handles rows b, b + G, b + 2G, ... (G = gridDim.x).  Its
-// k-th row contributes chunk 2k (gate, 2d bytes) and chunk 2k+1 (up); chunk c
-// lands in slot c mod S, guarded by mbarrier c mod S at phase parity (c / S)
-// mod 2.  Thread 0 refills a slot once every thread is past the barrier that
-// follows the slot's last read: at the first CTA barrier of row k, chunks up
-// to 2k are consumed (gate k is in registers, up k-1 was consumed by row
-// k-1's epilogue), so chunks up to 2k + S may be in flight.
+// Persistent CTAs.  Each CTA's j-th row contributes chunk 2j (gate, 2d bytes)
+// and chunk 2j+1 (up); chunk c lands in slot c mod S, guarded by mbarrier
+// c mod S at phase parity (c / S) mod 2.  Thread 0 picks a CTA's rows as it
+// issues their gate chunks and records each in slot_row[] beside the data:
+//   * static  (sched == nullptr): rows b, b + G, b + 2G, ... (G = gridDim.x);
+//   * dynamic (sched = a zeroed workspace): row b first, then G + the next
+//     ticket of the counter sched[0], so SMs that stream faster take more
+//     rows and the launch ends evenly;
+// a row >= T ends the CTA: thread 0 completes that slot's phase with a plain
+// arrive and slot_row = -1 tells every thread to stop.  Thread 0 refills a
+// slot once every thread is past the barrier that follows the slot's last
+// read: at the first CTA barrier of row j, chunks up to 2j are consumed (gate
+// j is in registers, up j-1 was consumed by row j-1's epilogue), so chunks
+// up to 2j + S may be in flight.  In dynamic mode the last CTA to finish
+// (counter sched[1]) sets both counters back to zero.
 // withhold >= 0 (failure-handling tests only): every CTA skips issuing its
 // chunk number `withhold`, so the wait for it runs out after wait_ns.
 template <int NT, int V>
 __global__ void __launch_bounds__(NT, (1024 / NT) > 0 ? (1024 / NT) : 1)
 gelu_tma_rows(uint16_t *__restrict__ out, const uint16_t *__restrict__ in, int64_t T, int d,
-              int64_t rs, float z, int S, int64_t withhold, unsigned long long wait_ns) {
+              int64_t rs, float z, int S, unsigned long long *__restrict__ sched,
+              int64_t withhold, unsigned long long wait_ns) {
     constexpr int NW = NT / 32;
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ float red[2][NW];
+    __shared__ int64_t slot_row[kTmaMaxStages];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t chunk = 2u * static_cast<uint32_t>(d);
     const uint32_t base = smem_addr(smem);
     const uint32_t bars = base + static_cast<uint32_t>(S) * chunk;
     const int64_t G = gridDim.x;
-    const int64_t nrows = blockIdx.x < T ? (T - 1 - blockIdx.x) / G + 1 : 0;
-    const int64_t nchunks = 2 * nrows;
     const int nvec = d >> 3;
 
     if (tid == 0) {
@@ -362,17 +380,37 @@ gelu_tma_rows(uint16_t *__restrict__ out, const uint16_t *__restrict__ in, int64
     pdl_wait();
     pdl_trigger();
 
-    int64_t issued = 0;   // thread 0: next chunk to issue
+    // Ring positions advance one chunk at a time (slot = c mod S, parity =
+    // (c / S) mod 2), kept as counters instead of divisions.
+    const uint32_t nslots = static_cast<uint32_t>(S);
+    int64_t issued = 0;     // thread 0: next chunk to issue ...
+    uint32_t islot = 0;     // ... and its slot
+    int64_t claimed = 0;    // thread 0: rows taken so far ...
+    int64_t row_i = 0;      // ... the last of them ...
+    bool more = true;       // ... and whether another may follow
     auto issue_upto = [&](int64_t last) {
         if (tid != 0)
             return;
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        for (; issued < nchunks && issued <= last; ++issued) {
+        for (; more && issued <= last; ++issued) {
+            const uint32_t slot = islot;
+            islot = islot + 1 == nslots ? 0u : islot + 1;
+            if ((issued & 1) == 0) {   // a gate chunk: the CTA's next row
+                row_i = claimed == 0 ? static_cast<int64_t>(blockIdx.x)
+                        : sched ? G + static_cast<int64_t>(atomicAdd(sched, 1ull))
+                                : static_cast<int64_t>(blockIdx.x) + claimed * G;
+                ++claimed;
+                if (row_i >= T) {
+                    slot_row[slot] = -1;
+                    mbar_arrive(bars + 8u * slot);
+                    more = false;
+                    continue;
+                }
+                slot_row[slot] = row_i;
+            }
             if (issued == withhold)
                 continue;
-            const int64_t row = blockIdx.x + (issued >> 1) * G;
-            const uint16_t *src = in + row * rs + ((issued & 1) ? d : 0);
-            const uint32_t slot = static_cast<uint32_t>(issued % S);
+            const uint16_t *src = in + row_i * rs + ((issued & 1) ? d : 0);
             mbar_expect_tx(bars + 8u * slot, chunk);
             bulk_load(base + slot * chunk, src, chunk, bars + 8u * slot);
         }
@@ -380,12 +418,23 @@ gelu_tma_rows(uint16_t *__restrict__ out, const uint16_t *__restrict__ in, int64
     issue_upto(S - 1);
 
     bool bad = false;
+    uint32_t cslot = 0, cpar = 0;   // every thread: the next chunk to consume
+    auto consume = [&](uint32_t *slot, uint32_t *par) {
+        *slot = cslot;
+        *par = cpar;
+        if (++cslot == nslots) {
+            cslot = 0;
+            cpar ^= 1u;
+        }
+    };
     int64_t k = 0;
-    for (; k < nrows; ++k) {
-        const int64_t row = blockIdx.x + k * G;
-        const int64_t cg = 2 * k, cu = 2 * k + 1;
-        const uint32_t sg = static_cast<uint32_t>(cg % S), su = static_cast<uint32_t>(cu % S);
-        bad |= !mbar_wait(bars + 8u * sg, static_cast<uint32_t>((cg / S) & 1), wait_ns);
+    for (;; ++k) {
+        const int64_t cg = 2 * k;
+        uint32_t sg, pg, su, pu;
+        consume(&sg, &pg);
+        consume(&su, &pu);
+        bad |= !mbar_wait(bars + 8u * sg, pg, wait_ns);
+        const int64_t row = slot_row[sg];
 
         const uint4 *gs = reinterpret_cast<const uint4 *>(smem + static_cast<size_t>(sg) * chunk);
         uint4 g[V];
@@ -401,7 +450,9 @@ gelu_tma_rows(uint16_t *__restrict__ out, const uint16_t *__restrict__ in, int64
         float s = warp_sum(acc.x + acc.y);
         if (lane == 0)
             red[0][warp] = s;
-        if (__syncthreads_or(bad))
+        // Both exits are CTA-uniform: the vote, and the end mark that every
+        // thread read after the same completed phase.
+        if (__syncthreads_or(bad) || row < 0)
             break;
         s = warp_sum(lane < NW ? red[0][lane] : 0.f);
         issue_upto(cg + S);
@@ -417,7 +468,7 @@ gelu_tma_rows(uint16_t *__restrict__ out, const uint16_t *__restrict__ in, int64
         const float sd = __fsqrt_rn(__fdiv_rn(q, static_cast<float>(d)));
         const float cutoff = fmaf(sd, z, mean);
 
-        bad |= !mbar_wait(bars + 8u * su, static_cast<uint32_t>((cu / S) & 1), wait_ns);
+        bad |= !mbar_wait(bars + 8u * su, pu, wait_ns);
         if (!bad) {
             const uint4 *us = reinterpret_cast<const uint4 *>(smem + static_cast<size_t>(su) * chunk);
             uint16_t *op = out + row * static_cast<int64_t>(d);
@@ -429,15 +480,26 @@ gelu_tma_rows(uint16_t *__restrict__ out, const uint16_t *__restrict__ in, int64
             }
         }
     }
-    // Every thread reaches this vote (the break above is CTA-uniform).  If a
-    // wait gave up, record it and let thread 0 wait, bounded again, for every
-    // copy it issued that was not consumed (from the up half of the row before
-    // the one in progress), so none is in flight when the CTA exits.
+    // Every thread reaches this vote.  If a wait gave up, record it and let
+    // thread 0 wait, bounded again, for every copy it issued that was not
+    // consumed (from the up half of the row before the one in progress), so
+    // none is in flight when the CTA exits.
     if (__syncthreads_or(bad) && tid == 0) {
         atomicOr(&g_device_status, 1u);
         for (int64_t c = k > 0 ? 2 * k - 1 : 0; c < issued; ++c)
             mbar_wait(bars + 8u * static_cast<uint32_t>(c % S),
                       static_cast<uint32_t>((c / S) & 1), wait_ns);
+    }
+    // Dynamic mode: this CTA takes no more tickets; the last CTA out resets
+    // the workspace for the next launch (fences order the tickets before the
+    // exit count, and the exit count before the reset).
+    if (sched && tid == 0) {
+        __threadfence();
+        if (atomicAdd(sched + 1, 1ull) == static_cast<unsigned long long>(G) - 1) {
+            __threadfence();
+            atomicExch(sched, 0ull);
+            atomicExch(sched + 1, 0ull);
+        }
     }
 }
 
@@ -660,8 +722,8 @@ gelu_scalar_rows(void *__restrict__ out_, const void *__restrict__ in_, int64_t 
 using WarpFn = void (*)(uint16_t *, const uint16_t *, int64_t, int, int64_t, float);
 using CtaFn = void (*)(void *, const void *, int64_t, int, int64_t, float, int, int);
 using ScalarFn = void (*)(void *, const void *, int64_t, int64_t, int64_t, float);
-using TmaFn = void (*)(uint16_t *, const uint16_t *, int64_t, int, int64_t, float, int, int64_t,
-                      unsigned long long);
+using TmaFn = void (*)(uint16_t *, const uint16_t *, int64_t, int, int64_t, float, int,
+                      unsigned long long *, int64_t, unsigned long long);
 
 WarpFn warp_fn(int v) {
     switch (v) {
@@ -840,6 +902,7 @@ int make_plan(const void *out, const void *in, int64_t T, int64_t d, int64_t rs,
         return rc;
     if (variant < GATED_ACT_VARIANT_AUTO || variant > GATED_ACT_VARIANT_TMA_ROWS)
         return GATED_ACT_ERR_VARIANT;
+    const bool forced = variant != GATED_ACT_VARIANT_AUTO;
     // the warp-rows and TMA-rows kernels exist for plain bf16 only; bulk copies
     // from host memory are not used
     const bool cta_only = dtype != GATED_ACT_BF16 || native;
@@ -891,6 +954,7 @@ int make_plan(const void *out, const void *in, int64_t T, int64_t d, int64_t rs,
         q.stages = t_stages;
         q.smem_bytes = t_smem;
         q.grid = std::min<int64_t>(T, static_cast<int64_t>(sms) * t_cps);
+        q.dynamic_rows = (forced || T >= kDynamicRowsPerCta * q.grid) ? 1 : 0;
         return GATED_ACT_OK;
     }
 
@@ -973,8 +1037,10 @@ int ensure_smem_attr(TmaFn fn, int nt) {
     return GATED_ACT_OK;
 }
 
+// workspace: zeroed counters for dynamic rows (bulk-copy geometry with
+// dynamic_rows set), else ignored.
 int launch(const Plan &p, void *out, const void *in, int64_t T, int64_t d, int64_t rs,
-           double z, cudaStream_t stream, int64_t withhold = -1,
+           double z, cudaStream_t stream, void *workspace = nullptr, int64_t withhold = -1,
            unsigned long long wait_ns = kWaitLimitNs) {
     uint16_t *o = static_cast<uint16_t *>(out);
     const uint16_t *x = static_cast<const uint16_t *>(in);
@@ -991,8 +1057,10 @@ int launch(const Plan &p, void *out, const void *in, int64_t T, int64_t d, int64
         const int rc = ensure_smem_attr(fn, q.threads);
         if (rc != GATED_ACT_OK)
             return rc;
+        unsigned long long *sched =
+            q.dynamic_rows ? static_cast<unsigned long long *>(workspace) : nullptr;
         e = launch_kernel(fn, grid, block, static_cast<size_t>(q.smem_bytes), stream, 1, o, x, T,
-                          di, rs, zf, static_cast<int>(q.stages), withhold, wait_ns);
+                          di, rs, zf, static_cast<int>(q.stages), sched, withhold, wait_ns);
         break;
     }
     case GATED_ACT_VARIANT_WARP_ROWS:
@@ -1045,13 +1113,35 @@ extern "C" int gelu_and_mul_sparse_plan(const void *out, const void *in, int64_t
 
 namespace gact {
 namespace {
-// Validate, resolve host buffers, plan and launch one gelu_and_mul_sparse call.
+// Validate, resolve host buffers, plan and launch one gelu_and_mul_sparse
+// call.  ws: the caller's workspace (gelu_and_mul_sparse_ws) or nullptr.
 int run_gelu(void *out, const void *in, int64_t T, int64_t d, int64_t rs, double z, int dtype,
-             int variant, int cluster, bool native, cudaStream_t stream) {
+             int variant, int cluster, bool native, cudaStream_t stream,
+             void *ws = nullptr) {
     Plan p;
     int rc = make_plan(out, in, T, d, rs, dtype, variant, cluster, 0, true, &p, native);
-    if (rc != GATED_ACT_OK || T == 0)
+    if (rc != GATED_ACT_OK)
         return rc;
+    if (ws) {
+        if (!aligned(ws, 8))
+            return GATED_ACT_ERR_ALIGN;
+        const int elem = elem_bytes(dtype);
+        const uint64_t in_bytes = T > 0 ? elem * static_cast<uint64_t>((T - 1) * rs + 2 * d) : 0;
+        const uint64_t out_bytes = elem * static_cast<uint64_t>(T * d);
+        if (ranges_overlap(ws, kWorkspaceBytes, in, in_bytes) ||
+            ranges_overlap(ws, kWorkspaceBytes, out, out_bytes))
+            return GATED_ACT_ERR_OVERLAP;
+    }
+    if (T == 0)
+        return GATED_ACT_OK;
+    if (ws) {   // the counters are updated with atomics: device memory only
+        const void *dws;
+        bool hws;
+        if ((rc = resolve_ptr(ws, &dws, &hws)) != GATED_ACT_OK)
+            return rc;
+        if (hws)
+            return GATED_ACT_ERR_HOST;
+    }
     const void *dout, *din;
     bool hout, hin;
     if ((rc = resolve_ptr(out, &dout, &hout)) != GATED_ACT_OK ||
@@ -1062,7 +1152,7 @@ int run_gelu(void *out, const void *in, int64_t T, int64_t d, int64_t rs, double
         if (rc != GATED_ACT_OK)
             return rc;
     }
-    return launch(p, const_cast<void *>(dout), din, T, d, rs, z, stream);
+    return launch(p, const_cast<void *>(dout), din, T, d, rs, z, stream, ws);
 }
 }  // namespace
 }  // namespace gact
@@ -1093,6 +1183,17 @@ extern "C" int gelu_and_mul_sparse(void *out, const void *in, int64_t T, int64_t
                                      GATED_ACT_VARIANT_AUTO, 0, stream);
 }
 
+extern "C" size_t gelu_and_mul_sparse_workspace_bytes(void) { return gact::kWorkspaceBytes; }
+
+extern "C" int gelu_and_mul_sparse_ws(void *out, const void *in, int64_t T, int64_t d,
+                                      int64_t row_stride, double z, int dtype, int variant,
+                                      int cluster, void *workspace, cudaStream_t stream) {
+    if (!workspace)
+        return GATED_ACT_ERR_NULL;
+    return gact::run_gelu(out, in, T, d, row_stride, z, dtype, variant, cluster, false, stream,
+                          workspace);
+}
+
 extern "C" int gated_act_selftest_wait_timeout(void *out, const void *in, int64_t T, int64_t d,
                                               unsigned long long wait_ns, cudaStream_t stream) {
     if (wait_ns == 0 || wait_ns > gact::kWaitLimitNs)
@@ -1103,7 +1204,7 @@ extern "C" int gated_act_selftest_wait_timeout(void *out, const void *in, int64_
     if (rc != GATED_ACT_OK || T == 0)
         return rc;
     // chunk 1 is the up half of each CTA's first row
-    return gact::launch(p, out, in, T, d, 2 * d, 1.0, stream, 1, wait_ns);
+    return gact::launch(p, out, in, T, d, 2 * d, 1.0, stream, nullptr, 1, wait_ns);
 }
 
 extern "C" int gated_act_device_status(unsigned int *flags) {

@@ -50,6 +50,7 @@
 #ifndef GATED_ACT_H
 #define GATED_ACT_H
 
+#include <stddef.h>
 #include <stdint.h>
 #include <cuda_runtime_api.h>
 
@@ -214,7 +215,9 @@ typedef struct gated_act_plan {
     int32_t stages;         /* shared-memory slots per CTA (TMA rows), else 0 */
     int32_t ctas_per_sm;    /* resident CTAs per SM the grid is sized for
                                (TMA rows), else 0                              */
-    int32_t reserved;
+    int32_t dynamic_rows;   /* 1: with a workspace (gelu_and_mul_sparse_ws)
+                               the bulk-copy CTAs take rows from an atomic
+                               counter; 0: rows are assigned round-robin    */
     int64_t grid;           /* CTAs launched                                   */
     int64_t smem_bytes;     /* dynamic shared memory per CTA                   */
 } gated_act_plan;
@@ -288,6 +291,45 @@ int gelu_and_mul_sparse_typed(void *out, const void *in, int64_t T, int64_t d,
 int gelu_and_mul_sparse_native(void *out, const void *in, int64_t T, int64_t d,
                                int64_t row_stride, double z, int dtype,
                                cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Dynamic rows through a caller-owned workspace.
+ *
+ * The bulk-copy geometry runs one persistent CTA (or a few) per SM.  Given
+ * round-robin rows, each CTA ends when its own share is done, and the SMs
+ * that stream more slowly set the end of the launch.  With a workspace the
+ * CTAs instead take rows from an atomic counter in it, so every SM stays
+ * busy to the end.  The results are identical: every row is still computed
+ * by one CTA in the same order.
+ * ------------------------------------------------------------------------ */
+
+/* Bytes of workspace gelu_and_mul_sparse_ws needs (a constant, 16). */
+size_t gelu_and_mul_sparse_workspace_bytes(void);
+
+/*
+ * gelu_and_mul_sparse_typed with a workspace.
+ *   workspace  device (or managed) memory of
+ *              gelu_and_mul_sparse_workspace_bytes() bytes, 8-byte aligned,
+ *              disjoint from in and out, all zero before its first use.
+ *              A call that completes leaves it all zero again, so one
+ *              workspace serves any number of calls that run one after
+ *              another on the GPU (one stream, or streams ordered by events;
+ *              replays of one CUDA graph are ordered too).  Calls that may
+ *              overlap on the GPU need workspaces of their own: two running
+ *              launches sharing one would take each other's row tickets.
+ *              The library only reads and writes it from the GPU.
+ *   Other arguments as gelu_and_mul_sparse_typed.  Rows are taken
+ *   dynamically when the plan's dynamic_rows is 1: the bulk-copy geometry
+ *   at six or more rows per CTA, or whenever it is forced; other geometries
+ *   ignore the workspace.
+ * Errors as gelu_and_mul_sparse_typed, plus GATED_ACT_ERR_NULL (no
+ * workspace), GATED_ACT_ERR_ALIGN (not 8-byte aligned), GATED_ACT_ERR_OVERLAP
+ * (it overlaps in or out) and GATED_ACT_ERR_HOST (host memory).
+ */
+int gelu_and_mul_sparse_ws(void *out, const void *in, int64_t T, int64_t d,
+                           int64_t row_stride, double z, int dtype,
+                           int variant, int cluster, void *workspace,
+                           cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -232,3 +232,34 @@ def test_plan_depends_only_on_arguments(lib):
     assert rc == 0 and p["variant"] == "tma_rows" and p["grid"] == 32
     rc, p = plan(lib, 1024, 32768, sms=512)
     assert rc == 0 and p["variant"] == "cta_row"
+
+
+def test_workspace_entry_rejects_bad_workspaces(lib):
+    assert lib.gelu_and_mul_sparse_workspace_bytes() == 16
+    # no workspace, or one that is not 8-byte aligned: refused before any launch
+    assert lib.gelu_and_mul_sparse_ws(0x1000, 0x100000, 4, 8, 16, 1.0, ga.BF16, 0, 0,
+                                      None, None) == ga.ERR_NULL
+    assert lib.gelu_and_mul_sparse_ws(0x1000, 0x100000, 0, 8, 16, 1.0, ga.BF16, 0, 0,
+                                      0x2004, None) == ga.ERR_ALIGN
+    # sizes are validated before the workspace
+    assert lib.gelu_and_mul_sparse_ws(0x1000, 0x100000, -1, 8, 16, 1.0, ga.BF16, 0, 0,
+                                      0x2000, None) == ga.ERR_SIZE
+
+
+def test_plan_reports_dynamic_rows(lib):
+    # d = 32768 bf16 on a 152-SM device: one bulk-copy CTA per SM; rows are
+    # taken dynamically (given a workspace) from six rows per CTA on
+    for T, dyn in ((456, 0), (911, 0), (912, 1), (2048, 1)):
+        p = ga.Plan()
+        assert lib.gelu_and_mul_sparse_plan(0x1000, 0x10000000, T, 32768, 65536, ga.BF16, 0, 0,
+                                            152, ctypes.byref(p)) == ga.OK
+        assert p.variant == ga.VARIANT_TMA_ROWS and p.grid == 152
+        assert p.dynamic_rows == dyn, (T, p.dynamic_rows)
+    # a forced bulk-copy geometry always takes rows dynamically; others never
+    p = ga.Plan()
+    assert lib.gelu_and_mul_sparse_plan(0x1000, 0x10000000, 10, 4096, 8192, ga.BF16,
+                                        ga.VARIANT_TMA_ROWS, 0, 152, ctypes.byref(p)) == ga.OK
+    assert p.dynamic_rows == 1
+    assert lib.gelu_and_mul_sparse_plan(0x1000, 0x10000000, 10, 4096, 8192, ga.BF16,
+                                        ga.VARIANT_CTA_ROW, 1, 152, ctypes.byref(p)) == ga.OK
+    assert p.dynamic_rows == 0
