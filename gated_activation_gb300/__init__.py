@@ -22,6 +22,7 @@ LIB_PATH = _build.LIB
 OK = 0
 ERR_NULL, ERR_SIZE, ERR_STRIDE, ERR_TOO_LARGE = -1, -2, -3, -4
 ERR_OVERLAP, ERR_VARIANT, ERR_CUDA, ERR_ALIGN, ERR_DTYPE, ERR_HOST = -5, -6, -7, -8, -9, -10
+ERR_SCRATCH = -11
 
 BF16, F16, F32 = 0, 1, 2
 _DTYPE_CODE = {torch.bfloat16: BF16, torch.float16: F16, torch.float32: F32}
@@ -36,6 +37,7 @@ EXPORTED = (
     "gated_act_device_status", "gated_act_noop", "gated_act_selftest_wait_timeout",
     "silu_and_mul_bounded", "gelu_and_mul",
     "squared_relu", "gelu_and_mul_sparse_workspace_bytes", "gelu_and_mul_sparse_ws",
+    "gelu_and_mul_sparse_ws_static",
 )
 
 
@@ -115,6 +117,9 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.gelu_and_mul_sparse_ws.argtypes = [vp, cvp, i64, i64, i64, ctypes.c_double, ctypes.c_int,
                                            ctypes.c_int, ctypes.c_int, vp, vp]
     lib.gelu_and_mul_sparse_ws.restype = ctypes.c_int
+    lib.gelu_and_mul_sparse_ws_static.argtypes = [vp, cvp, i64, i64, i64, ctypes.c_double,
+                                                  ctypes.c_int, ctypes.c_int, ctypes.c_int, vp]
+    lib.gelu_and_mul_sparse_ws_static.restype = ctypes.c_int
     if path is None:
         _lib = lib
     return lib

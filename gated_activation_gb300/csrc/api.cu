@@ -100,6 +100,7 @@ extern "C" const char *gated_act_status_string(int status) {
     case GATED_ACT_ERR_ALIGN: return "pointer is not aligned to its element size";
     case GATED_ACT_ERR_DTYPE: return "unknown or unsupported element type";
     case GATED_ACT_ERR_HOST: return "memory the CUDA runtime does not know (pageable or unallocated)";
+    case GATED_ACT_ERR_SCRATCH: return "needs more scratch than the library's static array holds";
     default: return "unknown status";
     }
 }

@@ -1194,6 +1194,69 @@ extern "C" int gelu_and_mul_sparse_ws(void *out, const void *in, int64_t T, int6
                           workspace);
 }
 
+// ------------------------------------------------------------ no-allocation variant
+// gelu_and_mul_sparse_ws_static serves callers that cannot allocate device
+// memory at all: an engine that reserved every free byte for its own pool at
+// start-up, or a plugin host that hands a kernel nothing but its inputs and
+// outputs.  For them even 16 bytes from cudaMalloc may fail, and cudaMalloc
+// and cudaFree may synchronize the device.  So the row counters live in this
+// library's own scratch array below.
+namespace gact {
+// 256 bytes on every GPU that loads the library, kept until the process
+// exits; a call needs the first kWorkspaceBytes of it.  In host code this name
+// is only a stand-in for the device array, never its address: host code gets
+// the address from cudaGetSymbolAddress.
+constexpr size_t kStaticScratchBytes = 256;
+static __device__ __align__(256) unsigned long long g_static_scratch[kStaticScratchBytes / 8];
+
+namespace {
+// Device address of g_static_scratch on the current device, looked up once per
+// device (the first call on a device does it).
+int static_scratch(void **addr) {
+    constexpr int kMaxDevices = 64;
+    static std::atomic<void *> cached[kMaxDevices];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_status(e);
+    void *p = (dev >= 0 && dev < kMaxDevices) ? cached[dev].load(std::memory_order_acquire)
+                                              : nullptr;
+    if (!p) {
+        e = cudaGetSymbolAddress(&p, g_static_scratch);
+        if (e != cudaSuccess)
+            return cuda_status(e);
+        if (dev >= 0 && dev < kMaxDevices)
+            cached[dev].store(p, std::memory_order_release);
+    }
+    *addr = p;
+    return GATED_ACT_OK;
+}
+}  // namespace
+}  // namespace gact
+
+extern "C" int gelu_and_mul_sparse_ws_static(void *out, const void *in, int64_t T, int64_t d,
+                                             int64_t row_stride, double z, int dtype,
+                                             int variant, int cluster, cudaStream_t stream) {
+    gact::Plan p;
+    int rc = gact::make_plan(out, in, T, d, row_stride, dtype, variant, cluster, 0, true, &p);
+    if (rc != GATED_ACT_OK || T == 0)
+        return rc;
+    // scratch this call needs: the row counters, when rows are taken dynamically
+    const size_t need = p.pub.dynamic_rows ? gact::kWorkspaceBytes : 0;
+    if (need > gact::kStaticScratchBytes)
+        return GATED_ACT_ERR_SCRATCH;
+    void *scratch = nullptr;
+    if ((rc = gact::static_scratch(&scratch)) != GATED_ACT_OK)
+        return rc;
+    // every call shares the array: start from zeroed counters whatever the
+    // last call left
+    const cudaError_t e = cudaMemsetAsync(scratch, 0, gact::kWorkspaceBytes, stream);
+    if (e != cudaSuccess)
+        return gact::cuda_status(e);
+    return gact::run_gelu(out, in, T, d, row_stride, z, dtype, variant, cluster, false, stream,
+                          scratch);
+}
+
 extern "C" int gated_act_selftest_wait_timeout(void *out, const void *in, int64_t T, int64_t d,
                                               unsigned long long wait_ns, cudaStream_t stream) {
     if (wait_ns == 0 || wait_ns > gact::kWaitLimitNs)

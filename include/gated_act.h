@@ -69,7 +69,8 @@ typedef enum gated_act_status {
     GATED_ACT_ERR_CUDA = -7,       /* the CUDA runtime reported an error at launch */
     GATED_ACT_ERR_ALIGN = -8,      /* a pointer is not aligned to its element size */
     GATED_ACT_ERR_DTYPE = -9,      /* unknown element type                        */
-    GATED_ACT_ERR_HOST = -10       /* memory the CUDA runtime does not know       */
+    GATED_ACT_ERR_HOST = -10,      /* memory the CUDA runtime does not know       */
+    GATED_ACT_ERR_SCRATCH = -11    /* more scratch than the static array holds    */
 } gated_act_status;
 
 /* Element types of the typed entry point (in and out share one type). */
@@ -330,6 +331,35 @@ int gelu_and_mul_sparse_ws(void *out, const void *in, int64_t T, int64_t d,
                            int64_t row_stride, double z, int dtype,
                            int variant, int cluster, void *workspace,
                            cudaStream_t stream);
+
+/*
+ * gelu_and_mul_sparse_ws_static -- gelu_and_mul_sparse_ws for callers that
+ * cannot allocate device memory.  The paper has no counterpart to this entry
+ * point.  Some callers cannot call cudaMalloc at all: an inference engine
+ * that reserved every free byte for its own pool at start-up, or a plugin
+ * host that hands a kernel only its inputs and outputs.  For them even a
+ * 16-byte workspace is out of reach, and cudaMalloc/cudaFree may also
+ * synchronize the device.  This entry point allocates nothing.  Its row
+ * counters live in a 256-byte scratch array inside the library, which every
+ * GPU that loads the library holds until the process exits.
+ *   Arguments as gelu_and_mul_sparse_ws, without the workspace.  The caller
+ *   still owns in and out.
+ *   The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture.
+ *   Every call shares the one array per device.  Each call first zeroes the
+ *   counters on `stream`, then launches.  Calls that overlap on the GPU
+ *   (other streams, other threads) race on the counters and can hand rows to
+ *   the wrong launch: order such calls on the GPU, or use
+ *   gelu_and_mul_sparse_ws with a workspace each.
+ *   A call that would need more scratch than the array holds returns
+ *   GATED_ACT_ERR_SCRATCH.  This op needs 16 bytes at any size.
+ * Results and other errors as gelu_and_mul_sparse_ws.
+ */
+int gelu_and_mul_sparse_ws_static(void *out, const void *in, int64_t T,
+                                  int64_t d, int64_t row_stride, double z,
+                                  int dtype, int variant, int cluster,
+                                  cudaStream_t stream);
 
 #ifdef __cplusplus
 }

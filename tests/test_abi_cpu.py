@@ -45,7 +45,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for code in range(-10, 1):
+    for code in range(-11, 1):
         s = lib.gated_act_status_string(code)
         assert s and s.decode()
     assert lib.gated_act_status_string(-99).decode() == "unknown status"
