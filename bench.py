@@ -592,26 +592,40 @@ def run_e2e(args, launches, host_in, world, local, dev) -> dict:
     for _ in range(2):
         step()
     torch.cuda.synchronize()
-    barrier(world, local)
     cur = torch.cuda.current_stream()
-    a = torch.cuda.Event(enable_timing=True)
-    b = torch.cuda.Event(enable_timing=True)
-    a.record(cur)
-    for s in (s_in, s_comp, s_out):
-        s.wait_event(a)
-    for _ in range(steps):
-        step()
-    for s in (s_in, s_comp, s_out):
-        cur.wait_stream(s)
-    b.record(cur)
-    torch.cuda.synchronize()
-    barrier(world, local)
-    ms = max_over_ranks(a.elapsed_time(b) / steps, world, dev)
+
+    def timed() -> float:
+        barrier(world, local)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(cur)
+        for s in (s_in, s_comp, s_out):
+            s.wait_event(a)
+        for _ in range(steps):
+            step()
+        for s in (s_in, s_comp, s_out):
+            cur.wait_stream(s)
+        b.record(cur)
+        torch.cuda.synchronize()
+        barrier(world, local)
+        return max_over_ranks(a.elapsed_time(b) / steps, world, dev)
+
+    return _e2e_record(launches, world, steps, h2d, d2h, timed,
+                       pipeline="3 streams: H2D / kernels / D2H, pinned host buffers")
+
+
+E2E_REPS = 3
+
+
+def _e2e_record(launches, world, steps, h2d, d2h, timed, **extra) -> dict:
+    """Time `steps` end-to-end steps E2E_REPS times; the line carries the
+    median (host memory traffic of other tenants moves single runs by 10-20%)."""
+    reps = sorted(timed() for _ in range(E2E_REPS))
+    ms = reps[len(reps) // 2]
     bytes_step = sum(L["bytes"] for L in launches)
     return {"value": round(world * bytes_step / (ms * 1e-3) / 1e9, 1), "unit": UNIT,
-            "ms_per_step": round(ms, 4), "steps": steps,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "pipeline": "3 streams: H2D / kernels / D2H, pinned host buffers"}
+            "ms_per_step": round(ms, 4), "steps": steps, "reps_ms": [round(r, 4) for r in reps],
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, **extra}
 
 
 def link_ceiling(h2d: int, d2h: int, dev) -> dict:
@@ -686,22 +700,22 @@ def run_e2e_host_direct(args, launches, host_in, world, local, dev) -> dict:
     for _ in range(2):
         step()
     torch.cuda.synchronize()
-    barrier(world, local)
-    a = torch.cuda.Event(enable_timing=True)
-    b = torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(steps):
-        step()
-    b.record()
-    torch.cuda.synchronize()
-    barrier(world, local)
-    ms = max_over_ranks(a.elapsed_time(b) / steps, world, dev)
-    bytes_step = sum(L["bytes"] for L in launches)
-    return {"value": round(world * bytes_step / (ms * 1e-3) / 1e9, 1), "unit": UNIT,
-            "ms_per_step": round(ms, 4), "steps": steps,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "transfer": "kernels read the inputs from and write the results to page-locked "
-                        "host buffers in place (NVLink-C2C); no copy is issued"}
+
+    def timed() -> float:
+        barrier(world, local)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(steps):
+            step()
+        b.record()
+        torch.cuda.synchronize()
+        barrier(world, local)
+        return max_over_ranks(a.elapsed_time(b) / steps, world, dev)
+
+    return _e2e_record(launches, world, steps, h2d, d2h, timed,
+                       transfer="kernels read the inputs from and write the results to "
+                                "page-locked host buffers in place (NVLink-C2C); no copy is issued")
 
 
 # ----------------------------------------------------------------- the oracle on host cores
