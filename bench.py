@@ -62,9 +62,13 @@ def shard_rows(T: int, world: int, rank: int) -> tuple[int, int]:
     return start, base + (1 if rank < extra else 0)
 
 
-def workload_launches(only: tuple | None = None) -> list[dict]:
-    """The step's launch list: gelu over (z, T, d), then silu over M."""
+def workload_launches(only: tuple | None = None, only_silu: int | None = None) -> list[dict]:
+    """The step's launch list: gelu over (z, T, d), then silu over M.  `only`
+    keeps one gelu shape, `only_silu` one silu row count (profiling runs)."""
     import workloads as W
+    if only_silu:
+        return [{"op": "silu", "T": only_silu, "d": W.SILU_D, "z": None,
+                 "bytes": silu_bytes(only_silu, W.SILU_D)}]
     out = []
     for z in W.SWEEP_Z:
         for T in W.SWEEP_T:
@@ -410,7 +414,7 @@ def run_ours(args, world, rank, local):
 
     torch.cuda.set_device(local)
     dev = f"cuda:{local}"
-    launches = workload_launches(args.only)
+    launches = workload_launches(args.only, args.only_silu)
     peaks = load_peaks()
 
     # inputs: seeded on the CPU and copied once to HBM; every launch has its own
@@ -435,7 +439,8 @@ def run_ours(args, world, rank, local):
         _launch(ga, L, dev_in[i], dev_out[i])
     torch.cuda.synchronize()
 
-    shapes, floor_us = per_shape_times(ga, launches + ([] if args.only else extra_launches()),
+    profiling = bool(args.only or args.only_silu)
+    shapes, floor_us = per_shape_times(ga, launches + ([] if profiling else extra_launches()),
                                        dev, peaks["hbm_gbs"]) \
         if not args.no_per_shape else ([], None)
     shapes_step = [r for r in shapes if r["op"] in ("gelu", "silu")]
@@ -528,7 +533,9 @@ def run_ours(args, world, rank, local):
             "config": {"workload": "gelu_and_mul_sparse sweep T{1,8,64,256,1024,2048} x "
                                    "d{2048,4096,8192,16384,32768} x z{0,1.6448536269514722} "
                                    "+ silu_and_mul MoE decode M{1024,2048,4096,16384} d768"
-                       if not args.only else f"gelu_and_mul_sparse T={args.only[0]} d={args.only[1]}",
+                       if not profiling else (f"gelu_and_mul_sparse T={args.only[0]} d={args.only[1]}"
+                                              if args.only else
+                                              f"silu_and_mul M={args.only_silu} d={launches[0]['d']}"),
                        "launches_per_step": len(launches), "bytes_per_step": bytes_step,
                        "math": "fp32 on bf16 storage",
                        "rows": "gelu launches pass a workspace: the persistent bulk-copy "
@@ -754,7 +761,7 @@ def run_reference(args, world, rank):
         return
     import oracle
     o = oracle.default()
-    launches = workload_launches(args.only)
+    launches = workload_launches(args.only, args.only_silu)
     host_in = {}
     for L in launches:
         key = (L["op"], L["T"], L["d"])
@@ -807,6 +814,8 @@ def parse_args(argv=None):
     ap.add_argument("--only", type=lambda s: tuple(float(v) if "." in v else int(v)
                                                    for v in s.split(",")), default=None,
                     help="time one gelu shape T,d[,z] (profiling); not a bench line")
+    ap.add_argument("--only-silu", type=int, default=None, metavar="M",
+                    help="time one silu_and_mul row count M (profiling); not a bench line")
     a = ap.parse_args(argv)
     if a.warmup < 3 and a.impl == "ours":
         ap.error("--warmup must be >= 3")
