@@ -143,3 +143,17 @@ def test_workspace_argument_checks(ga):
     assert call(pageable.ctypes.data) == ga.ERR_HOST
     torch.cuda.synchronize()
     assert (buf == 0).all().item()
+
+
+def test_workspace_with_host_buffers_is_ignored(ga, oracle):
+    # page-locked host rows never take the bulk-copy geometry, so the
+    # workspace is not used and stays zeroed
+    inp = W.iid(2048, 16384, seed=21)
+    x = inp.x.pin_memory()
+    ws = ga.new_workspace()
+    assert ga.gelu_and_mul_sparse_plan(x)["dynamic_rows"] == 0
+    out = ga.gelu_and_mul_sparse(x, inp.z, workspace=ws)
+    torch.cuda.synchronize()
+    assert not out.is_cuda and _zeroed(ws)
+    res = oracle.gelu_and_mul_sparse(W.to_bits(inp.x), d=16384, z=inp.z)
+    check_gelu(out, inp.x, 16384, res, "host rows with a workspace")
