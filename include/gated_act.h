@@ -224,11 +224,13 @@ typedef struct gated_act_plan {
 } gated_act_plan;
 
 /*
- * Describe the launch gelu_and_mul_sparse(_ex, _typed) would make, without
- * launching.  dtype a gated_act_dtype; variant/cluster as in
- * gelu_and_mul_sparse_ex; out/in are only inspected for
- * alignment (never dereferenced).  sm_count > 0 plans for a device with that
- * many SMs; sm_count <= 0 queries the current device (its only CUDA call).
+ * Describe the launch gelu_and_mul_sparse(_ex, _typed, _ws) would make,
+ * without launching.  dtype a gated_act_dtype; variant/cluster as in
+ * gelu_and_mul_sparse_ex.  out/in are never dereferenced: they are inspected
+ * for alignment, and classified with cudaPointerGetAttributes (page-locked
+ * host memory rules out the bulk-copy geometry; a pointer the runtime cannot
+ * classify, or 0 for out, plans as device memory).  sm_count > 0 plans for a
+ * device with that many SMs; sm_count <= 0 queries the current device.
  * Returns 0 and fills *plan, or a negative status (GATED_ACT_ERR_VARIANT when
  * the forced geometry does not fit).
  */
