@@ -13,7 +13,9 @@
 //   * tma rows    -- persistent CTAs; each streams its rows' gate and up halves
 //                    through a ring of shared-memory slots with 1-D bulk copies
 //                    (cp.async.bulk, completion on mbarriers), so HBM keeps
-//                    streaming while earlier rows are reduced and written;
+//                    streaming while earlier rows are reduced and written.
+//                    Rows go round-robin, or, given a workspace, to whichever
+//                    CTA takes the next ticket of an atomic counter;
 //   * warp rows   -- one warp per row, shuffles only (d <= 2048);
 //   * CTA row     -- one CTA per row, or a cluster of C CTAs per row, each CTA
 //                    holding a column slice in registers; CTA partials (count,
