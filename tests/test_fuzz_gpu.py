@@ -1,4 +1,4 @@
-"""Randomised GPU parity of gelu_and_mul_sparse.
+"""Randomised GPU parity of gelu_and_mul_sparse (and of its native-rounding mode).
 
 Seeded draws of everything the launch depends on are each checked against the
 fp64 oracle with the per-type tolerance of tests/parity.py:
@@ -89,3 +89,36 @@ def test_random_launch(ga, oracle, i):
     check_gelu(out, x, d, oracle_result(oracle, x, d, z), label)
     if c["const_row"]:
         assert torch.count_nonzero(out[T // 2].float()).item() == 0, label
+
+
+# ------------------------------------------------------------ native-rounding mode
+N_NATIVE = 60
+
+
+def draw_native(i: int) -> dict:
+    r = np.random.default_rng(60_000 + i)
+    dt = (torch.bfloat16, torch.float16)[int(r.integers(2))]
+    if r.random() < 0.75:
+        d = 8 * int(np.exp(r.uniform(0.0, np.log(4096))))
+        pad = 8 * int(r.integers(0, 3))
+    else:
+        d = int(np.exp(r.uniform(0.0, np.log(20000))))
+        pad = int(r.integers(0, 9))
+    d = max(d, 1)
+    T = max(1, int(min(MAX_ELEMS // d, np.exp(r.uniform(0.0, np.log(2048))))))
+    z = float(r.choice([0.0, W.Z95, 1.3, r.uniform(-1.0, 3.0)]))
+    return {"dtype": dt, "T": T, "d": d, "rs": 2 * d + pad, "z": z, "seed": 70_000 + i}
+
+
+@pytest.mark.parametrize("i", range(N_NATIVE))
+def test_random_native_launch(ga, oracle, i):
+    from tests.parity import check_native
+    c = draw_native(i)
+    T, d, z = c["T"], c["d"], c["z"]
+    x = W.iid(T, d, seed=c["seed"], row_stride=c["rs"], z=z, dtype=c["dtype"]).x
+    arr = W.to_bits(x) if x.dtype == torch.bfloat16 else x.contiguous().numpy()
+    ref, mask, cut = oracle.gelu_and_mul_sparse_native(arr, d=d, z=z,
+                                                       bf16_bits=x.dtype == torch.bfloat16)
+    out = ga.gelu_and_mul_sparse_native(x.cuda(), z, d=d)
+    torch.cuda.synchronize()
+    check_native(out.cpu(), x, d, ref, mask, cut, f"native case {i}: {c}")
