@@ -37,7 +37,7 @@ EXPORTED = (
     "gated_act_device_status", "gated_act_noop", "gated_act_selftest_wait_timeout",
     "silu_and_mul_bounded", "gelu_and_mul",
     "squared_relu", "gelu_and_mul_sparse_workspace_bytes", "gelu_and_mul_sparse_ws",
-    "gelu_and_mul_sparse_ws_static",
+    "gelu_and_mul_sparse_ws_static", "gated_act_selftest_wait_timeout_ws",
 )
 
 
@@ -106,6 +106,9 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.gated_act_noop.restype = ctypes.c_int
     lib.gated_act_selftest_wait_timeout.argtypes = [vp, cvp, i64, i64, ctypes.c_ulonglong, vp]
     lib.gated_act_selftest_wait_timeout.restype = ctypes.c_int
+    lib.gated_act_selftest_wait_timeout_ws.argtypes = [vp, cvp, i64, i64, ctypes.c_ulonglong,
+                                                       vp, vp]
+    lib.gated_act_selftest_wait_timeout_ws.restype = ctypes.c_int
     lib.silu_and_mul_bounded.argtypes = [vp, cvp, i64, i64, cvp, vp]
     lib.silu_and_mul_bounded.restype = ctypes.c_int
     lib.gelu_and_mul.argtypes = [vp, cvp, i64, i64, i64, vp]

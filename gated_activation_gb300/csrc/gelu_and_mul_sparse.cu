@@ -1272,6 +1272,25 @@ extern "C" int gated_act_selftest_wait_timeout(void *out, const void *in, int64_
     return gact::launch(p, out, in, T, d, 2 * d, 1.0, stream, nullptr, 1, wait_ns);
 }
 
+extern "C" int gated_act_selftest_wait_timeout_ws(void *out, const void *in, int64_t T,
+                                                 int64_t d, unsigned long long wait_ns,
+                                                 void *workspace, cudaStream_t stream) {
+    if (wait_ns == 0 || wait_ns > gact::kWaitLimitNs)
+        return GATED_ACT_ERR_SIZE;
+    if (!workspace)
+        return GATED_ACT_ERR_NULL;
+    if (!gact::aligned(workspace, 8))
+        return GATED_ACT_ERR_ALIGN;
+    gact::Plan p;
+    const int rc = gact::make_plan(out, in, T, d, 2 * d, GATED_ACT_BF16,
+                                   GATED_ACT_VARIANT_TMA_ROWS, 0, 0, true, &p);
+    if (rc != GATED_ACT_OK || T == 0)
+        return rc;
+    // forced geometry: rows are taken dynamically; chunk 1 is the up half of
+    // each CTA's first row
+    return gact::launch(p, out, in, T, d, 2 * d, 1.0, stream, workspace, 1, wait_ns);
+}
+
 extern "C" int gated_act_device_status(unsigned int *flags) {
     if (!flags)
         return GATED_ACT_ERR_NULL;

@@ -190,6 +190,17 @@ int gated_act_selftest_wait_timeout(void *out, const void *in, int64_t T,
                                     int64_t d, unsigned long long wait_ns,
                                     cudaStream_t stream);
 
+/*
+ * gated_act_selftest_wait_timeout with dynamic rows: the same withheld copy
+ * per CTA, with rows taken from `workspace` as in gelu_and_mul_sparse_ws
+ * (a zeroed device workspace of gelu_and_mul_sparse_workspace_bytes()).
+ * Every CTA still counts itself out on the give-up path, so the workspace is
+ * left zeroed for the next call.
+ */
+int gated_act_selftest_wait_timeout_ws(void *out, const void *in, int64_t T,
+                                       int64_t d, unsigned long long wait_ns,
+                                       void *workspace, cudaStream_t stream);
+
 /* ------------------------------------------------------------------------
  * Launch-geometry control, for tests and measurements.
  *

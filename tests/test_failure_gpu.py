@@ -46,3 +46,28 @@ def test_selftest_rejects_unbounded_limits(ga):
     assert lib.gated_act_selftest_wait_timeout(o.data_ptr(), x.data_ptr(), 4, 32, 0, None) == ga.ERR_SIZE
     assert lib.gated_act_selftest_wait_timeout(o.data_ptr(), x.data_ptr(), 4, 32, 2_000_000_000,
                                                None) == ga.ERR_SIZE
+
+
+def test_wait_runs_out_with_dynamic_rows(ga, oracle):
+    # rows taken from a workspace: every CTA gives up on its first row's up
+    # half, still counts itself out, and the last one resets the workspace
+    assert ga.device_status() == 0
+    inp = W.iid(2000, 4096, seed=12)      # more rows than CTAs: tickets are taken
+    x = inp.x.cuda()
+    out = torch.zeros((2000, 4096), dtype=torch.bfloat16, device="cuda")
+    ws = ga.new_workspace()
+    lib = ga.load_library()
+    rc = lib.gated_act_selftest_wait_timeout_ws(out.data_ptr(), x.data_ptr(), 2000, 4096,
+                                                20_000_000, ws.data_ptr(),
+                                                torch.cuda.current_stream().cuda_stream)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert ga.device_status() == 1
+    assert int(ws.count_nonzero().item()) == 0
+    good = ga.gelu_and_mul_sparse(x, inp.z, variant=ga.VARIANT_TMA_ROWS, workspace=ws)
+    torch.cuda.synchronize()
+    res = oracle.gelu_and_mul_sparse(W.to_bits(inp.x), d=4096, z=inp.z)
+    check_gelu(good.cpu(), inp.x, 4096, res, "dynamic rows after timeout")
+    assert int(ws.count_nonzero().item()) == 0 and ga.device_status() == 0
+    assert lib.gated_act_selftest_wait_timeout_ws(out.data_ptr(), x.data_ptr(), 4, 4096,
+                                                  20_000_000, None, None) == ga.ERR_NULL
