@@ -284,6 +284,8 @@ def kernel_name(plan: dict) -> str:
         return "gelu_scalar_rows"
     if v == "tma_rows":
         return f"gelu_tma_rows<{plan['threads']},4>"
+    if v == "pipe_rows":
+        return f"gelu_pipe_rows<{plan['threads'] // 32 - 1},{plan['vec_per_thread']}>"
     return v
 
 
@@ -430,7 +432,7 @@ def run_ours(args, world, rank, local):
         dev_out.append(torch.empty((L["T"], L["d"]), dtype=torch.bfloat16, device=dev))
     for i, L in enumerate(launches):
         if L["op"] == "gelu":
-            L["plan"] = ga.gelu_and_mul_sparse_plan(dev_in[i], d=L["d"])
+            L["plan"] = ga.gelu_and_mul_sparse_plan(dev_in[i], d=L["d"], workspace=True)
             L["kernel"] = kernel_name(L["plan"])
         else:
             L["plan"] = None

@@ -28,16 +28,19 @@ BF16, F16, F32 = 0, 1, 2
 _DTYPE_CODE = {torch.bfloat16: BF16, torch.float16: F16, torch.float32: F32}
 
 VARIANT_AUTO, VARIANT_WARP_ROWS, VARIANT_CTA_ROW, VARIANT_SCALAR, VARIANT_TMA_ROWS = 0, 1, 2, 3, 4
-VARIANT_NAMES = {0: "auto", 1: "warp_rows", 2: "cta_row", 3: "scalar", 4: "tma_rows"}
+VARIANT_PIPE_ROWS = 5
+VARIANT_NAMES = {0: "auto", 1: "warp_rows", 2: "cta_row", 3: "scalar", 4: "tma_rows", 5: "pipe_rows"}
 
 EXPORTED = (
     "gelu_and_mul_sparse", "gelu_and_mul_sparse_typed", "gelu_and_mul_sparse_native",
     "silu_and_mul", "gated_act_status_string",
-    "gated_act_last_cuda_error", "gelu_and_mul_sparse_plan", "gelu_and_mul_sparse_ex",
+    "gated_act_last_cuda_error", "gelu_and_mul_sparse_plan", "gelu_and_mul_sparse_plan_ex",
+    "gelu_and_mul_sparse_ex",
     "gated_act_device_status", "gated_act_noop", "gated_act_selftest_wait_timeout",
     "silu_and_mul_bounded", "gelu_and_mul",
     "squared_relu", "gelu_and_mul_sparse_workspace_bytes", "gelu_and_mul_sparse_ws",
     "gelu_and_mul_sparse_ws_static", "gated_act_selftest_wait_timeout_ws",
+    "gated_act_selftest_wait_timeout_ex",
 )
 
 
@@ -87,6 +90,10 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.gelu_and_mul_sparse_ex.restype = ctypes.c_int
     lib.gelu_and_mul_sparse_plan.argtypes = [cvp, cvp, i64, i64, i64, ctypes.c_int, ctypes.c_int,
                                              ctypes.c_int, ctypes.c_int, ctypes.POINTER(Plan)]
+    lib.gelu_and_mul_sparse_plan_ex.argtypes = [cvp, cvp, i64, i64, i64, ctypes.c_int,
+                                                ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                ctypes.c_int, ctypes.POINTER(Plan)]
+    lib.gelu_and_mul_sparse_plan_ex.restype = ctypes.c_int
     lib.gelu_and_mul_sparse_typed.argtypes = [vp, cvp, i64, i64, i64, ctypes.c_double,
                                               ctypes.c_int, ctypes.c_int, ctypes.c_int, vp]
     lib.gelu_and_mul_sparse_typed.restype = ctypes.c_int
@@ -109,6 +116,9 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.gated_act_selftest_wait_timeout_ws.argtypes = [vp, cvp, i64, i64, ctypes.c_ulonglong,
                                                        vp, vp]
     lib.gated_act_selftest_wait_timeout_ws.restype = ctypes.c_int
+    lib.gated_act_selftest_wait_timeout_ex.argtypes = [vp, cvp, i64, i64, ctypes.c_ulonglong,
+                                                       ctypes.c_int, vp, vp]
+    lib.gated_act_selftest_wait_timeout_ex.restype = ctypes.c_int
     lib.silu_and_mul_bounded.argtypes = [vp, cvp, i64, i64, cvp, vp]
     lib.silu_and_mul_bounded.restype = ctypes.c_int
     lib.gelu_and_mul.argtypes = [vp, cvp, i64, i64, i64, vp]
@@ -246,15 +256,18 @@ def gelu_and_mul_sparse_native(x: torch.Tensor, z: float, d: int | None = None,
 
 
 def gelu_and_mul_sparse_plan(x: torch.Tensor, d: int | None = None, out: torch.Tensor | None = None,
-                             variant: int = VARIANT_AUTO, cluster: int = 0) -> dict:
-    """The launch geometry gelu_and_mul_sparse would use for this call."""
+                             variant: int = VARIANT_AUTO, cluster: int = 0,
+                             workspace: bool = False) -> dict:
+    """The launch geometry gelu_and_mul_sparse would use for this call
+    (``workspace``: a call that passes a workspace)."""
     T, rs = _rows_view(x, tuple(_DTYPE_CODE))
     d = int(x.shape[1]) // 2 if d is None else d
     p = Plan()
     out_ptr = out.data_ptr() if out is not None else 0
-    rc = load_library().gelu_and_mul_sparse_plan(out_ptr, x.data_ptr(), T, d, rs,
-                                                 _DTYPE_CODE[x.dtype], int(variant), int(cluster),
-                                                 0, ctypes.byref(p))
+    rc = load_library().gelu_and_mul_sparse_plan_ex(out_ptr, x.data_ptr(), T, d, rs,
+                                                    _DTYPE_CODE[x.dtype], int(variant),
+                                                    int(cluster), 0, int(bool(workspace)),
+                                                    ctypes.byref(p))
     _check("gelu_and_mul_sparse_plan", rc)
     return p.as_dict()
 

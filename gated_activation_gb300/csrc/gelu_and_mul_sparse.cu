@@ -59,7 +59,7 @@ constexpr unsigned long long kWaitLimitNs = 1000000000ull;   // 1 s bound on eve
 // round-robin is as fast, since a CTA takes its next row about one row ahead
 // of need and the last claims can then leave one CTA a row behind).
 constexpr int64_t kDynamicRowsPerCta = 6;
-constexpr size_t kWorkspaceBytes = 16;                       // two 64-bit counters
+constexpr size_t kWorkspaceBytes = 16;   // a 64-bit row-ticket counter and 8 reserved bytes
 
 // ------------------------------------------------------------ paired fp32 math
 __device__ __forceinline__ unsigned long long u64_of(float2 v) {
@@ -352,8 +352,13 @@ __device__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned long long limi
 // slot once every thread is past the barrier that follows the slot's last
 // read: at the first CTA barrier of row j, chunks up to 2j are consumed (gate
 // j is in registers, up j-1 was consumed by row j-1's epilogue), so chunks
-// up to 2j + S may be in flight.  In dynamic mode the last CTA to finish
-// (counter sched[1]) sets both counters back to zero.
+// up to 2j + S may be in flight.  Thread 0 takes row j + 1's ticket at that
+// barrier and issues its copies after the second one, so the atomic's round
+// trip overlaps the variance reduction.
+// Dynamic mode resets its own counter with no exit protocol: every CTA stops
+// at its first failing ticket (G + t >= T), so a launch hands out exactly T
+// tickets, T - G of them rows and G of them stops, and the CTA that draws
+// ticket T - 1 is the last one to touch the counter; it sets it back to zero.
 // withhold >= 0 (failure-handling tests only): every CTA skips issuing its
 // chunk number `withhold`, so the wait for it runs out after wait_ns.
 template <int NT, int V>
@@ -390,6 +395,21 @@ gelu_tma_rows(uint16_t *__restrict__ out, const uint16_t *__restrict__ in, int64
     int64_t claimed = 0;    // thread 0: rows taken so far ...
     int64_t row_i = 0;      // ... the last of them ...
     bool more = true;       // ... and whether another may follow
+    // thread 0, dynamic mode: a ticket taken ahead of the copy that needs it
+    // (kNoTicket: none)
+    constexpr unsigned long long kNoTicket = ~0ull;
+    unsigned long long ticket = kNoTicket;
+    // Dynamic mode: the ticket that stops this CTA is the launch's last one
+    // (T - 1) for exactly one CTA, which sets the counter back to zero.
+    auto stop_ticket = [&](int64_t r) {
+        if (sched && r == G + T - 1)
+            asm volatile("red.relaxed.gpu.global.and.b64 [%0], %1;" ::"l"(sched), "l"(0ull)
+                         : "memory");
+    };
+    auto take_ticket = [&]() {
+        if (tid == 0 && sched && more && claimed > 0 && ticket == kNoTicket)
+            ticket = atomicAdd(sched, 1ull);
+    };
     auto issue_upto = [&](int64_t last) {
         if (tid != 0)
             return;
@@ -398,14 +418,21 @@ gelu_tma_rows(uint16_t *__restrict__ out, const uint16_t *__restrict__ in, int64
             const uint32_t slot = islot;
             islot = islot + 1 == nslots ? 0u : islot + 1;
             if ((issued & 1) == 0) {   // a gate chunk: the CTA's next row
-                row_i = claimed == 0 ? static_cast<int64_t>(blockIdx.x)
-                        : sched ? G + static_cast<int64_t>(atomicAdd(sched, 1ull))
-                                : static_cast<int64_t>(blockIdx.x) + claimed * G;
+                if (claimed == 0) {
+                    row_i = static_cast<int64_t>(blockIdx.x);
+                } else if (sched) {
+                    take_ticket();
+                    row_i = G + static_cast<int64_t>(ticket);
+                    ticket = kNoTicket;
+                } else {
+                    row_i = static_cast<int64_t>(blockIdx.x) + claimed * G;
+                }
                 ++claimed;
                 if (row_i >= T) {
                     slot_row[slot] = -1;
                     mbar_arrive(bars + 8u * slot);
                     more = false;
+                    stop_ticket(row_i);
                     continue;
                 }
                 slot_row[slot] = row_i;
@@ -457,7 +484,7 @@ gelu_tma_rows(uint16_t *__restrict__ out, const uint16_t *__restrict__ in, int64
         if (__syncthreads_or(bad) || row < 0)
             break;
         s = warp_sum(lane < NW ? red[0][lane] : 0.f);
-        issue_upto(cg + S);
+        take_ticket();   // its round trip overlaps the variance reduction
 
         const float mean = __fdiv_rn(s, static_cast<float>(d));
         const float2 m2 = make_float2(mean, mean);
@@ -467,6 +494,7 @@ gelu_tma_rows(uint16_t *__restrict__ out, const uint16_t *__restrict__ in, int64
             if (tid + NT * i < nvec)
                 acc = ssd_vec<FmtBf16>(acc, g[i], m2);
         const float q = block_sum<NW>(acc.x + acc.y, red[1], lane, warp);
+        issue_upto(cg + S);
         const float sd = __fsqrt_rn(__fdiv_rn(q, static_cast<float>(d)));
         const float cutoff = fmaf(sd, z, mean);
 
@@ -492,16 +520,237 @@ gelu_tma_rows(uint16_t *__restrict__ out, const uint16_t *__restrict__ in, int64
             mbar_wait(bars + 8u * static_cast<uint32_t>(c % S),
                       static_cast<uint32_t>((c / S) & 1), wait_ns);
     }
-    // Dynamic mode: this CTA takes no more tickets; the last CTA out resets
-    // the workspace for the next launch (fences order the tickets before the
-    // exit count, and the exit count before the reset).
-    if (sched && tid == 0) {
-        __threadfence();
-        if (atomicAdd(sched + 1, 1ull) == static_cast<unsigned long long>(G) - 1) {
-            __threadfence();
-            atomicExch(sched, 0ull);
-            atomicExch(sched + 1, 0ull);
+    // Dynamic mode, a CTA that stopped before its failing ticket (it gave
+    // up): it draws tickets until one fails, so the launch still hands out
+    // exactly T and the counter is reset by whichever CTA draws T - 1.
+    if (sched && tid == 0 && more) {
+        int64_t r = ticket != kNoTicket ? G + static_cast<int64_t>(ticket) : -1;
+        while (r < T)
+            r = G + static_cast<int64_t>(atomicAdd(sched, 1ull));
+        stop_ticket(r);
+    }
+}
+
+// ------------------------------------------------------------ pipe rows
+// Persistent CTAs with one producer lane and NCW consumer warps.  The
+// consumers hold a row's gate in registers (V 16-byte vectors per thread)
+// and finish the row; lane 0 of the last warp streams gate and up half-rows
+// into a ring of S shared-memory slots with bulk copies and picks the CTA's
+// rows (round-robin, or tickets from the workspace counter as in tma rows).
+// Slot s has a "full" mbarrier (the producer's arrive plus the copy's bytes)
+// and an "empty" one (one arrive per consumer warp once the slot has been
+// read), so copy issue and ticket round trips run beside the consumers, who
+// synchronise among themselves with a named barrier only.  Chunk c (gate of
+// the CTA's row c/2 for even c, up for odd c) uses slot c mod S.
+// Failure handling: every wait is bounded.  Consumers that give up vote to
+// stop together and leave their slots unreleased; the producer notices
+// (cons_done), stops issuing, and waits (bounded) for its own copies in
+// flight -- the latest use of each slot -- before it exits.
+template <int NCW>
+__device__ __forceinline__ void cons_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(NCW * 32) : "memory");
+}
+template <int NCW>
+__device__ __forceinline__ bool cons_sync_or(bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n bar.red.or.pred p, 1, %2, q;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred)), "n"(NCW * 32)
+        : "memory");
+    return r != 0;
+}
+template <int NCW>
+__device__ __forceinline__ float cons_sum(float v, float *red, int lane, int warp) {
+    v = warp_sum(v);
+    if (lane == 0)
+        red[warp] = v;
+    cons_sync<NCW>();
+    return warp_sum(lane < NCW ? red[lane] : 0.f);
+}
+
+constexpr int kPipeMaxStages = 16;
+
+template <int NCW, int V>
+__global__ void __launch_bounds__((NCW + 1) * 32, (NCW >= 16 ? 1 : NCW >= 8 ? 2 : 4))
+gelu_pipe_rows(uint16_t *__restrict__ out, const uint16_t *__restrict__ in, int64_t T, int d,
+               int64_t rs, float z, int S, unsigned long long *__restrict__ sched,
+               int64_t withhold, unsigned long long wait_ns) {
+    constexpr int NC = NCW * 32;
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ float red[2][NCW];
+    __shared__ int cons_done;   // consumers have left their loop
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t chunk = 2u * static_cast<uint32_t>(d);
+    const uint32_t base = smem_addr(smem);
+    const uint32_t full = base + static_cast<uint32_t>(S) * chunk;
+    const uint32_t empty = full + 8u * static_cast<uint32_t>(S);
+    int64_t *slot_row = reinterpret_cast<int64_t *>(smem + static_cast<size_t>(S) * chunk +
+                                                    16u * static_cast<uint32_t>(S));
+    const uint32_t nslots = static_cast<uint32_t>(S);
+    const int nvec = d >> 3;
+
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full + 8u * s, 1);
+            mbar_init(empty + 8u * s, NCW);
         }
+        cons_done = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    pdl_wait();
+    pdl_trigger();
+
+    if (warp == NCW) {
+        // ---------------- producer (one lane)
+        if (lane != 0)
+            return;
+        const int64_t G = gridDim.x;
+        volatile int *done = &cons_done;
+        // the consumers' release of a slot, or false once they have stopped
+        // (or after a limit well past theirs)
+        auto wait_empty = [&](uint32_t bar, uint32_t par) -> bool {
+            if (mbar_try_wait(bar, par))
+                return true;
+            const unsigned long long t0 = globaltimer_ns();
+            for (uint32_t i = 1;; ++i) {
+                if (mbar_try_wait(bar, par))
+                    return true;
+                if ((i & 63u) == 0 && (*done || globaltimer_ns() - t0 > 3 * wait_ns))
+                    return false;
+            }
+        };
+        int64_t c = 0, row = 0, claimed = 0;
+        uint32_t slot = 0, round = 0;
+        bool ended = false, bad = false;
+        for (;; ++c) {
+            if (round > 0 && !wait_empty(empty + 8u * slot, (round - 1) & 1u)) {
+                bad = true;
+                break;
+            }
+            if ((c & 1) == 0) {   // a gate chunk: the CTA's next row
+                row = claimed == 0 ? static_cast<int64_t>(blockIdx.x)
+                      : sched      ? G + static_cast<int64_t>(atomicAdd(sched, 1ull))
+                                   : static_cast<int64_t>(blockIdx.x) + claimed * G;
+                ++claimed;
+                if (row >= T) {
+                    slot_row[slot] = -1;
+                    mbar_arrive(full + 8u * slot);
+                    if (sched && row == G + T - 1)   // ticket T - 1: reset the counter
+                        asm volatile("red.relaxed.gpu.global.and.b64 [%0], %1;" ::"l"(sched),
+                                     "l"(0ull)
+                                     : "memory");
+                    ended = true;
+                    break;
+                }
+                slot_row[slot] = row;
+            }
+            if (c != withhold) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                mbar_expect_tx(full + 8u * slot, chunk);
+                bulk_load(base + slot * chunk, in + row * rs + ((c & 1) ? d : 0), chunk,
+                          full + 8u * slot);
+            }
+            if (++slot == nslots) {
+                slot = 0;
+                ++round;
+            }
+        }
+        // No copy may be in flight when the CTA exits: wait for the latest
+        // copy into each slot (chunks c - S .. c - 1; after a normal end,
+        // chunk c - S was released before the end mark took its slot).
+        for (int64_t x = c - S + (ended ? 1 : 0); x < c; ++x)
+            if (x >= 0 && x != withhold)
+                bad |= !mbar_wait(full + 8u * static_cast<uint32_t>(x % S),
+                                  static_cast<uint32_t>((x / S) & 1), wait_ns);
+        if (bad)
+            atomicOr(&g_device_status, 1u);
+        // dynamic rows, stopped early: draw tickets until the first failing
+        // one, so the launch hands out exactly T and one CTA resets the counter
+        if (sched && !ended) {
+            int64_t r = -1;
+            while (r < T)
+                r = G + static_cast<int64_t>(atomicAdd(sched, 1ull));
+            if (r == G + T - 1)
+                asm volatile("red.relaxed.gpu.global.and.b64 [%0], %1;" ::"l"(sched), "l"(0ull)
+                             : "memory");
+        }
+        return;
+    }
+
+    // ---------------- consumers
+    bool bad = false;
+    uint32_t cslot = 0, cpar = 0;
+    auto next = [&](uint32_t *s, uint32_t *p) {
+        *s = cslot;
+        *p = cpar;
+        if (++cslot == nslots) {
+            cslot = 0;
+            cpar ^= 1u;
+        }
+    };
+    for (;;) {
+        uint32_t sg, pg, su, pu;
+        next(&sg, &pg);
+        next(&su, &pu);
+        bad |= !mbar_wait(full + 8u * sg, pg, wait_ns);
+        const int64_t row = slot_row[sg];
+        const uint4 *gs = reinterpret_cast<const uint4 *>(smem + static_cast<size_t>(sg) * chunk);
+        uint4 g[V];
+#pragma unroll
+        for (int i = 0; i < V; ++i) {
+            const int v = tid + NC * i;
+            g[i] = v < nvec ? gs[v] : make_uint4(0u, 0u, 0u, 0u);
+        }
+        float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < V; ++i)
+            acc = sum_vec<FmtBf16>(acc, g[i]);
+        float s = warp_sum(acc.x + acc.y);
+        if (lane == 0)
+            red[0][warp] = s;
+        // both exits are uniform over the consumers: the vote, and the end
+        // mark every consumer read after the same completed phase
+        if (cons_sync_or<NCW>(bad) || row < 0)
+            break;
+        if (lane == 0)
+            mbar_arrive(empty + 8u * sg);   // the gate half-row is in registers
+        s = warp_sum(lane < NCW ? red[0][lane] : 0.f);
+
+        const float mean = __fdiv_rn(s, static_cast<float>(d));
+        const float2 m2 = make_float2(mean, mean);
+        acc = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < V; ++i)
+            if (tid + NC * i < nvec)
+                acc = ssd_vec<FmtBf16>(acc, g[i], m2);
+        const float q = cons_sum<NCW>(acc.x + acc.y, red[1], lane, warp);
+        const float sd = __fsqrt_rn(__fdiv_rn(q, static_cast<float>(d)));
+        const float cutoff = fmaf(sd, z, mean);
+
+        bad |= !mbar_wait(full + 8u * su, pu, wait_ns);
+        if (!bad) {
+            const uint4 *us = reinterpret_cast<const uint4 *>(smem + static_cast<size_t>(su) * chunk);
+            uint16_t *op = out + row * static_cast<int64_t>(d);
+#pragma unroll
+            for (int i = 0; i < V; ++i) {
+                const int v = tid + NC * i;
+                if (v < nvec)
+                    st_vec(op + 8 * v, epi_vec<FmtBf16>(g[i], us[v], cutoff));
+            }
+        }
+        // a warp that missed the up half-row keeps its slot (its copy may
+        // still land); the vote at the next row stops everyone
+        if (!__any_sync(0xFFFFFFFFu, bad) && lane == 0)
+            mbar_arrive(empty + 8u * su);
+    }
+    if (tid == 0) {
+        if (bad)
+            atomicOr(&g_device_status, 1u);
+        *static_cast<volatile int *>(&cons_done) = 1;
     }
 }
 
@@ -801,6 +1050,20 @@ TmaFn tma_fn(int nt) {
     }
 }
 
+// Pipe rows: NCW consumer warps x V gate vectors per consumer thread.
+TmaFn pipe_fn(int ncw, int v) {
+    switch (ncw * 16 + v) {
+    case 16 * 16 + 8: return gelu_pipe_rows<16, 8>;
+    case 16 * 16 + 4: return gelu_pipe_rows<16, 4>;
+    case 8 * 16 + 8: return gelu_pipe_rows<8, 8>;
+    case 8 * 16 + 4: return gelu_pipe_rows<8, 4>;
+    case 4 * 16 + 8: return gelu_pipe_rows<4, 8>;
+    case 4 * 16 + 4: return gelu_pipe_rows<4, 4>;
+    case 4 * 16 + 2: return gelu_pipe_rows<4, 2>;
+    default: return nullptr;
+    }
+}
+
 int pow2_ceil(int64_t x) {
     int p = 1;
     while (p < x)
@@ -851,6 +1114,55 @@ bool tma_shape_for(int64_t nvec, int c, int *nt, int *stages, int64_t *smem) {
     return true;
 }
 
+// Pipe rows geometry for a row of nvec gate vectors at cps CTAs per SM:
+// consumer warps and vectors per thread from the instantiated set (four
+// vectors per thread preferred), no more CTAs per SM than the kernel's
+// register budget allows (its launch bounds), and at least three ring slots
+// in 1/cps of the SM's shared memory.
+bool pipe_shape_for(int64_t nvec, int cps, int *ncw, int *v, int *stages, int64_t *smem) {
+    static const int kShapes[][2] = {{4, 4}, {8, 4}, {16, 4}, {4, 8}, {8, 8}, {16, 8}, {4, 2}};
+    for (const auto &sh : kShapes) {
+        const int w = sh[0], vv = sh[1];
+        const int64_t cap = int64_t(w) * 32 * vv;
+        if (cap < nvec || (w > 4 && cap / 2 >= nvec))
+            continue;   // too small, or a smaller CTA would do
+        if (cps > (w >= 16 ? 1 : w >= 8 ? 2 : 4))
+            continue;   // the register budget each kernel is compiled for
+        const int64_t chunk = 16 * nvec;
+        const int64_t per_cta = std::min<int64_t>(kTmaSmemPerSm / cps, kTmaSmemPerCta) - 1536;
+        const int64_t s = std::min<int64_t>(kPipeMaxStages, per_cta / (chunk + 24));
+        if (s < 3)
+            continue;
+        *ncw = w;
+        *v = vv;
+        *stages = static_cast<int>(s);
+        *smem = s * (chunk + 24);
+        return true;
+    }
+    return false;
+}
+
+bool pipe_shape(int64_t nvec, int want_cps, int *cps, int *ncw, int *v, int *stages,
+                int64_t *smem) {
+    if (want_cps > 0) {
+        if (want_cps > 8 || (want_cps & (want_cps - 1)) != 0)
+            return false;
+        *cps = want_cps;
+        return pipe_shape_for(nvec, want_cps, ncw, v, stages, smem);
+    }
+    // default: as many CTAs per SM as keep 16 KB or more of each row's gate
+    // per CTA in flight: 16384 / d rows' worth
+    for (int c = 8; c >= 1; c /= 2) {
+        if (16 * nvec * c > 16 * 2048 * 2 && c > 1)
+            continue;
+        if (pipe_shape_for(nvec, c, ncw, v, stages, smem)) {
+            *cps = c;
+            return true;
+        }
+    }
+    return false;
+}
+
 bool tma_shape(int64_t nvec, int want_cps, int *cps, int *nt, int *stages, int64_t *smem) {
     if (want_cps > 0) {
         if (want_cps > 16 || (want_cps & (want_cps - 1)) != 0)
@@ -895,23 +1207,23 @@ int validate(const void *out, const void *in, int64_t T, int64_t d, int64_t rs, 
 // host_mem: in or out lives in host memory; only register-load kernels run.
 int make_plan(const void *out, const void *in, int64_t T, int64_t d, int64_t rs, int dtype,
               int variant, int cluster, int sm_count, bool check_ptrs, Plan *p,
-              bool native = false, bool host_mem = false) {
+              bool native = false, bool host_mem = false, bool has_ws = false) {
     if (dtype < GATED_ACT_BF16 || dtype > GATED_ACT_F32 || (native && dtype == GATED_ACT_F32))
         return GATED_ACT_ERR_DTYPE;
     const int elem = elem_bytes(dtype), epv = 16 / elem;
     const int rc = validate(out, in, T, d, rs, elem, check_ptrs);
     if (rc != GATED_ACT_OK)
         return rc;
-    if (variant < GATED_ACT_VARIANT_AUTO || variant > GATED_ACT_VARIANT_TMA_ROWS)
+    if (variant < GATED_ACT_VARIANT_AUTO || variant > GATED_ACT_VARIANT_PIPE_ROWS)
         return GATED_ACT_ERR_VARIANT;
     const bool forced = variant != GATED_ACT_VARIANT_AUTO;
     // the warp-rows and TMA-rows kernels exist for plain bf16 only; bulk copies
     // from host memory are not used
     const bool cta_only = dtype != GATED_ACT_BF16 || native;
-    if (cta_only &&
-        (variant == GATED_ACT_VARIANT_WARP_ROWS || variant == GATED_ACT_VARIANT_TMA_ROWS))
+    const bool bulk = variant == GATED_ACT_VARIANT_TMA_ROWS || variant == GATED_ACT_VARIANT_PIPE_ROWS;
+    if (cta_only && (variant == GATED_ACT_VARIANT_WARP_ROWS || bulk))
         return GATED_ACT_ERR_VARIANT;
-    if (host_mem && variant == GATED_ACT_VARIANT_TMA_ROWS)
+    if (host_mem && bulk)
         return GATED_ACT_ERR_VARIANT;
     gated_act_plan &q = p->pub;
     q = gated_act_plan{};
@@ -926,15 +1238,29 @@ int make_plan(const void *out, const void *in, int64_t T, int64_t d, int64_t rs,
     const int want_cps = variant == GATED_ACT_VARIANT_TMA_ROWS ? cluster : 0;
     const bool tma_ok = vec_ok && !cta_only && !host_mem &&
                         tma_shape(nvec, want_cps, &t_cps, &t_nt, &t_stages, &t_smem);
+    int p_cps = 0, p_ncw = 0, p_v = 0, p_stages = 0;
+    int64_t p_smem = 0;
+    const bool pipe_ok =
+        vec_ok && !cta_only && !host_mem &&
+        pipe_shape(nvec, variant == GATED_ACT_VARIANT_PIPE_ROWS ? cluster : 0, &p_cps, &p_ncw,
+                   &p_v, &p_stages, &p_smem);
 
     // Measured on GB300 (every geometry timed per T x d, graph-replayed over
-    // rotating buffers): persistent TMA rows win only for the widest rows at
-    // many rows per SM; one CTA per row wins everywhere else, except a handful
-    // of rows of d >= 16384, where 8-CTA clusters put more SMs on each row.
+    // rotating buffers):
+    //  * rows wider than 16384 from about 1.6 rows per SM at d = 32768 on:
+    //    pipe rows; with a workspace (dynamic rows) at any T, without one
+    //    while round-robin rows stay below 8 per CTA (d = 32768; beyond that
+    //    a slow SM holds the static split back more than in tma rows);
+    //  * tma rows for the widest rows at many rows per SM;
+    //  * one CTA per row everywhere else, except a handful of rows of
+    //    d >= 16384, where 8-CTA clusters put more SMs on each row.
     if (variant == GATED_ACT_VARIANT_AUTO) {
         const int64_t sm = static_cast<int64_t>(sms);
         if (!vec_ok || nvec > int64_t(kMaxSliceVec) * kMaxCluster)
             variant = GATED_ACT_VARIANT_SCALAR;
+        else if (pipe_ok && nvec > 2048 && 10 * T * nvec >= 16 * sm * 4096 &&
+                 (has_ws || nvec < 4096 || T < 8 * sm))
+            variant = GATED_ACT_VARIANT_PIPE_ROWS;
         else if (tma_ok && ((nvec >= 4096 && T >= 3 * sm) || (nvec >= 2048 && T >= 12 * sm)))
             variant = GATED_ACT_VARIANT_TMA_ROWS;
         else if (nvec <= 64 && !cta_only)
@@ -957,6 +1283,22 @@ int make_plan(const void *out, const void *in, int64_t T, int64_t d, int64_t rs,
         q.smem_bytes = t_smem;
         q.grid = std::min<int64_t>(T, static_cast<int64_t>(sms) * t_cps);
         q.dynamic_rows = (forced || T >= kDynamicRowsPerCta * q.grid) ? 1 : 0;
+        return GATED_ACT_OK;
+    }
+
+    if (variant == GATED_ACT_VARIANT_PIPE_ROWS) {
+        if (!pipe_ok)
+            return GATED_ACT_ERR_VARIANT;
+        q.variant = variant;
+        q.cluster = 1;
+        q.threads = (p_ncw + 1) * 32;
+        q.vec_per_thread = p_v;
+        q.rows_per_cta = 1;
+        q.ctas_per_sm = p_cps;
+        q.stages = p_stages;
+        q.smem_bytes = p_smem;
+        q.grid = std::min<int64_t>(T, static_cast<int64_t>(sms) * p_cps);
+        q.dynamic_rows = 1;   // measured: never slower than round-robin here
         return GATED_ACT_OK;
     }
 
@@ -1015,13 +1357,14 @@ int make_plan(const void *out, const void *in, int64_t T, int64_t d, int64_t rs,
 
 // Shared memory above 48 KB needs a per-kernel opt-in, done once per device;
 // the carveout hint asks for the largest shared-memory split of L1.
-int ensure_smem_attr(TmaFn fn, int nt) {
+// key: a bit index in [0, 32) that names the kernel.
+int ensure_smem_attr(TmaFn fn, int key) {
     constexpr int kMaxDevices = 64;
     static std::atomic<unsigned> done[kMaxDevices];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess)
         dev = -1;
-    const unsigned bit = 1u << (31 - __builtin_clz(static_cast<unsigned>(nt)));
+    const unsigned bit = 1u << key;
     if (dev >= 0 && dev < kMaxDevices && (done[dev].load(std::memory_order_acquire) & bit))
         return GATED_ACT_OK;
     cudaFuncAttributes fa;
@@ -1056,7 +1399,21 @@ int launch(const Plan &p, void *out, const void *in, int64_t T, int64_t d, int64
         TmaFn fn = tma_fn(q.threads);
         if (!fn)
             return GATED_ACT_ERR_VARIANT;
-        const int rc = ensure_smem_attr(fn, q.threads);
+        const int rc = ensure_smem_attr(fn, 31 - __builtin_clz(static_cast<unsigned>(q.threads)));
+        if (rc != GATED_ACT_OK)
+            return rc;
+        unsigned long long *sched =
+            q.dynamic_rows ? static_cast<unsigned long long *>(workspace) : nullptr;
+        e = launch_kernel(fn, grid, block, static_cast<size_t>(q.smem_bytes), stream, 1, o, x, T,
+                          di, rs, zf, static_cast<int>(q.stages), sched, withhold, wait_ns);
+        break;
+    }
+    case GATED_ACT_VARIANT_PIPE_ROWS: {
+        const int ncw = q.threads / 32 - 1;
+        TmaFn fn = pipe_fn(ncw, q.vec_per_thread);
+        if (!fn)
+            return GATED_ACT_ERR_VARIANT;
+        const int rc = ensure_smem_attr(fn, 16 + ncw / 4 + q.vec_per_thread);
         if (rc != GATED_ACT_OK)
             return rc;
         unsigned long long *sched =
@@ -1089,9 +1446,10 @@ int launch(const Plan &p, void *out, const void *in, int64_t T, int64_t d, int64
 }  // namespace
 }  // namespace gact
 
-extern "C" int gelu_and_mul_sparse_plan(const void *out, const void *in, int64_t T, int64_t d,
-                                        int64_t row_stride, int dtype, int variant, int cluster,
-                                        int sm_count, gated_act_plan *plan) {
+extern "C" int gelu_and_mul_sparse_plan_ex(const void *out, const void *in, int64_t T,
+                                           int64_t d, int64_t row_stride, int dtype, int variant,
+                                           int cluster, int sm_count, int with_workspace,
+                                           gated_act_plan *plan) {
     if (!plan)
         return GATED_ACT_ERR_NULL;
     // A buffer in page-locked host memory rules out the bulk-copy geometry, as
@@ -1106,11 +1464,18 @@ extern "C" int gelu_and_mul_sparse_plan(const void *out, const void *in, int64_t
     }
     gact::Plan p;
     const int rc = gact::make_plan(out, in, T, d, row_stride, dtype, variant, cluster, sm_count,
-                                   false, &p, false, host);
+                                   false, &p, false, host, with_workspace != 0);
     if (rc != GATED_ACT_OK)
         return rc;
     *plan = p.pub;
     return GATED_ACT_OK;
+}
+
+extern "C" int gelu_and_mul_sparse_plan(const void *out, const void *in, int64_t T, int64_t d,
+                                        int64_t row_stride, int dtype, int variant, int cluster,
+                                        int sm_count, gated_act_plan *plan) {
+    return gelu_and_mul_sparse_plan_ex(out, in, T, d, row_stride, dtype, variant, cluster,
+                                       sm_count, 0, plan);
 }
 
 namespace gact {
@@ -1121,7 +1486,8 @@ int run_gelu(void *out, const void *in, int64_t T, int64_t d, int64_t rs, double
              int variant, int cluster, bool native, cudaStream_t stream,
              void *ws = nullptr) {
     Plan p;
-    int rc = make_plan(out, in, T, d, rs, dtype, variant, cluster, 0, true, &p, native);
+    int rc = make_plan(out, in, T, d, rs, dtype, variant, cluster, 0, true, &p, native, false,
+                       ws != nullptr);
     if (rc != GATED_ACT_OK)
         return rc;
     if (ws) {
@@ -1150,7 +1516,8 @@ int run_gelu(void *out, const void *in, int64_t T, int64_t d, int64_t rs, double
         (rc = resolve_ptr(in, &din, &hin)) != GATED_ACT_OK)
         return rc;
     if (hout || hin) {
-        rc = make_plan(dout, din, T, d, rs, dtype, variant, cluster, 0, true, &p, native, true);
+        rc = make_plan(dout, din, T, d, rs, dtype, variant, cluster, 0, true, &p, native, true,
+                       ws != nullptr);
         if (rc != GATED_ACT_OK)
             return rc;
     }
@@ -1240,7 +1607,8 @@ extern "C" int gelu_and_mul_sparse_ws_static(void *out, const void *in, int64_t 
                                              int64_t row_stride, double z, int dtype,
                                              int variant, int cluster, cudaStream_t stream) {
     gact::Plan p;
-    int rc = gact::make_plan(out, in, T, d, row_stride, dtype, variant, cluster, 0, true, &p);
+    int rc = gact::make_plan(out, in, T, d, row_stride, dtype, variant, cluster, 0, true, &p,
+                             false, false, true);
     if (rc != GATED_ACT_OK || T == 0)
         return rc;
     // scratch this call needs: the row counters, when rows are taken dynamically
@@ -1288,6 +1656,25 @@ extern "C" int gated_act_selftest_wait_timeout_ws(void *out, const void *in, int
         return rc;
     // forced geometry: rows are taken dynamically; chunk 1 is the up half of
     // each CTA's first row
+    return gact::launch(p, out, in, T, d, 2 * d, 1.0, stream, workspace, 1, wait_ns);
+}
+
+extern "C" int gated_act_selftest_wait_timeout_ex(void *out, const void *in, int64_t T,
+                                                 int64_t d, unsigned long long wait_ns,
+                                                 int variant, void *workspace,
+                                                 cudaStream_t stream) {
+    if (wait_ns == 0 || wait_ns > gact::kWaitLimitNs)
+        return GATED_ACT_ERR_SIZE;
+    if (variant != GATED_ACT_VARIANT_TMA_ROWS && variant != GATED_ACT_VARIANT_PIPE_ROWS)
+        return GATED_ACT_ERR_VARIANT;
+    if (workspace && !gact::aligned(workspace, 8))
+        return GATED_ACT_ERR_ALIGN;
+    gact::Plan p;
+    const int rc = gact::make_plan(out, in, T, d, 2 * d, GATED_ACT_BF16, variant, 0, 0, true, &p);
+    if (rc != GATED_ACT_OK || T == 0)
+        return rc;
+    // forced geometry: with a workspace rows are taken dynamically; chunk 1
+    // is the up half of each CTA's first row
     return gact::launch(p, out, in, T, d, 2 * d, 1.0, stream, workspace, 1, wait_ns);
 }
 

@@ -194,12 +194,30 @@ int gated_act_selftest_wait_timeout(void *out, const void *in, int64_t T,
  * gated_act_selftest_wait_timeout with dynamic rows: the same withheld copy
  * per CTA, with rows taken from `workspace` as in gelu_and_mul_sparse_ws
  * (a zeroed device workspace of gelu_and_mul_sparse_workspace_bytes()).
- * Every CTA still counts itself out on the give-up path, so the workspace is
- * left zeroed for the next call.
+ * A CTA that gives up still draws row tickets until its first failing one,
+ * so the launch hands out its usual number and the workspace is left zeroed
+ * for the next call.
  */
 int gated_act_selftest_wait_timeout_ws(void *out, const void *in, int64_t T,
                                        int64_t d, unsigned long long wait_ns,
                                        void *workspace, cudaStream_t stream);
+
+/*
+ * The same self-test for either bulk-copy geometry: variant is
+ * GATED_ACT_VARIANT_TMA_ROWS or GATED_ACT_VARIANT_PIPE_ROWS (the library's
+ * choice of CTAs per SM); workspace is null (round-robin rows) or a zeroed
+ * workspace (dynamic rows).  In the pipe-rows geometry the consumer warps
+ * give up on the withheld copy, vote to stop together and leave their slots
+ * unreleased; the producer lane sees that, stops issuing, waits (bounded)
+ * for the copies it issued that may still be landing, and, with dynamic
+ * rows, draws tickets until its first failing one so the workspace is left
+ * zeroed.  Errors as gated_act_selftest_wait_timeout_ws, plus
+ * GATED_ACT_ERR_VARIANT for any other variant.
+ */
+int gated_act_selftest_wait_timeout_ex(void *out, const void *in, int64_t T,
+                                       int64_t d, unsigned long long wait_ns,
+                                       int variant, void *workspace,
+                                       cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
  * Launch-geometry control, for tests and measurements.
@@ -214,8 +232,11 @@ typedef enum gated_act_variant {
     GATED_ACT_VARIANT_CTA_ROW = 2,   /* one CTA, or a cluster of CTAs, per row;
                                         row held in registers                       */
     GATED_ACT_VARIANT_SCALAR = 3,    /* any layout: one CTA per row, 2-byte loads   */
-    GATED_ACT_VARIANT_TMA_ROWS = 4   /* persistent CTAs; gate/up half-rows stream
+    GATED_ACT_VARIANT_TMA_ROWS = 4,  /* persistent CTAs; gate/up half-rows stream
                                         through shared memory by bulk copy          */
+    GATED_ACT_VARIANT_PIPE_ROWS = 5  /* as TMA_ROWS, with one producer lane that
+                                        issues the copies and picks rows while the
+                                        other warps finish rows                      */
 } gated_act_variant;
 
 typedef struct gated_act_plan {
@@ -224,9 +245,10 @@ typedef struct gated_act_plan {
     int32_t threads;        /* threads per CTA                                 */
     int32_t vec_per_thread; /* 16-byte vectors of gate per thread (0: scalar)  */
     int32_t rows_per_cta;   /* rows one CTA handles at a time                  */
-    int32_t stages;         /* shared-memory slots per CTA (TMA rows), else 0 */
+    int32_t stages;         /* shared-memory slots per CTA (TMA and pipe
+                               rows), else 0                                   */
     int32_t ctas_per_sm;    /* resident CTAs per SM the grid is sized for
-                               (TMA rows), else 0                              */
+                               (TMA and pipe rows), else 0                     */
     int32_t dynamic_rows;   /* 1: with a workspace (gelu_and_mul_sparse_ws)
                                the bulk-copy CTAs take rows from an atomic
                                counter; 0: rows are assigned round-robin    */
@@ -235,8 +257,8 @@ typedef struct gated_act_plan {
 } gated_act_plan;
 
 /*
- * Describe the launch gelu_and_mul_sparse(_ex, _typed, _ws) would make,
- * without launching.  dtype a gated_act_dtype; variant/cluster as in
+ * Describe the launch gelu_and_mul_sparse(_ex, _typed) would make, without
+ * launching.  dtype a gated_act_dtype; variant/cluster as in
  * gelu_and_mul_sparse_ex.  out/in are never dereferenced: they are inspected
  * for alignment, and classified with cudaPointerGetAttributes (page-locked
  * host memory rules out the bulk-copy geometry; a pointer the runtime cannot
@@ -251,16 +273,29 @@ int gelu_and_mul_sparse_plan(const void *out, const void *in, int64_t T,
                              gated_act_plan *plan);
 
 /*
+ * gelu_and_mul_sparse_plan for either kind of call: with_workspace = 0 the
+ * plain call (as gelu_and_mul_sparse_plan), nonzero a call with a workspace
+ * (gelu_and_mul_sparse_ws or gelu_and_mul_sparse_ws_static), whose automatic
+ * choice may differ (see "Dynamic rows" below).
+ */
+int gelu_and_mul_sparse_plan_ex(const void *out, const void *in, int64_t T,
+                                int64_t d, int64_t row_stride, int dtype,
+                                int variant, int cluster, int sm_count,
+                                int with_workspace, gated_act_plan *plan);
+
+/*
  * gelu_and_mul_sparse with a forced geometry.
  *   variant  a gated_act_variant; AUTO behaves like gelu_and_mul_sparse.
- *            TMA_ROWS needs the 16-byte layout and d <= 32768; the first
- *            TMA_ROWS launch of a kernel shape on a device raises that
+ *            TMA_ROWS and PIPE_ROWS need the 16-byte layout and d <= 32768;
+ *            the first launch of such a kernel shape on a device raises that
  *            kernel's shared-memory limit (cudaFuncSetAttribute), so make one
  *            call per device before capturing such launches in a graph.
  *   cluster  for GATED_ACT_VARIANT_CTA_ROW: CTAs per row, a power of two
  *            in [1, 8]; for GATED_ACT_VARIANT_TMA_ROWS: CTAs per SM, a power
- *            of two in [1, 16] (threads per CTA = 1024 / that); 0 lets the
- *            library choose; ignored by the other variants.
+ *            of two in [1, 16] (threads per CTA = 1024 / that); for
+ *            GATED_ACT_VARIANT_PIPE_ROWS: CTAs per SM, a power of two in
+ *            [1, 8]; 0 lets the library choose; ignored by the other
+ *            variants.
  * Returns GATED_ACT_ERR_VARIANT when the layout cannot use that geometry
  * (vector variants need the 16-byte layout above; a row slice must fit the
  * CTA's registers).
@@ -309,12 +344,16 @@ int gelu_and_mul_sparse_native(void *out, const void *in, int64_t T, int64_t d,
 /* ------------------------------------------------------------------------
  * Dynamic rows through a caller-owned workspace.
  *
- * The bulk-copy geometry runs one persistent CTA (or a few) per SM.  Given
+ * The bulk-copy geometries run one persistent CTA (or a few) per SM.  Given
  * round-robin rows, each CTA ends when its own share is done, and the SMs
  * that stream more slowly set the end of the launch.  With a workspace the
  * CTAs instead take rows from an atomic counter in it, so every SM stays
- * busy to the end.  The results are identical: every row is still computed
- * by one CTA in the same order.
+ * busy to the end.  Within one geometry the results are identical: every row
+ * is still computed by one CTA in the same order.  The automatic choice can
+ * differ with a workspace: for rows wider than 16384 it prefers pipe rows,
+ * which gain most from dynamic rows, where the plain call keeps tma rows
+ * (d = 32768 from 8 rows per SM on).  Then the two calls agree within the
+ * accuracy bound rather than bitwise; gelu_and_mul_sparse_plan_ex tells.
  * ------------------------------------------------------------------------ */
 
 /* Bytes of workspace gelu_and_mul_sparse_ws needs (a constant, 16). */

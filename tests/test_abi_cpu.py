@@ -130,8 +130,11 @@ def test_plan_geometry_families(lib):
     rc, p = plan(lib, 2048, 16384)
     assert rc == 0 and p["variant"] == "tma_rows" and p["grid"] <= 16 * GB300_SMS
     assert p["stages"] >= 2 and p["smem_bytes"] <= 227 * 1024
-    rc, p = plan(lib, 512, 32768)
+    rc, p = plan(lib, 2048, 32768)
     assert rc == 0 and p["variant"] == "tma_rows" and p["threads"] == 1024
+    # rows wider than 16384 at fewer rows per SM: the producer/consumer rows
+    rc, p = plan(lib, 512, 32768)
+    assert rc == 0 and p["variant"] == "pipe_rows" and p["threads"] == 544
     rc, p = plan(lib, 1024, 16384)
     assert rc == 0 and p["variant"] == "cta_row" and p["threads"] == 512
     # a handful of wide rows: 8-CTA clusters per row
@@ -156,6 +159,10 @@ def test_plan_covers_every_slice(lib):
                 # every CTA of an SM fits: slots of 2d bytes plus their barriers
                 assert p["smem_bytes"] == p["stages"] * (2 * d + 8)
                 assert p["stages"] >= 2 and p["smem_bytes"] <= 227 * 1024 - 1024
+            elif p["variant"] == "pipe_rows":
+                # consumer threads (all warps but the producer's) cover the row
+                assert (p["threads"] - 32) * p["vec_per_thread"] >= nvec
+                assert p["smem_bytes"] == p["stages"] * (2 * d + 24) and p["stages"] >= 3
             elif p["variant"] == "cta_row":
                 sv = -(-nvec // p["cluster"])
                 assert p["threads"] * p["vec_per_thread"] >= sv
@@ -228,9 +235,9 @@ def test_plan_depends_only_on_arguments(lib):
     b = plan(lib, 64, 8192)
     assert a == b
     # a different SM count may change the choice, never the validity
-    rc, p = plan(lib, 1024, 32768, sms=32)
+    rc, p = plan(lib, 2048, 32768, sms=32)
     assert rc == 0 and p["variant"] == "tma_rows" and p["grid"] == 32
-    rc, p = plan(lib, 1024, 32768, sms=512)
+    rc, p = plan(lib, 1024, 32768, sms=1024)
     assert rc == 0 and p["variant"] == "cta_row"
 
 
@@ -247,14 +254,16 @@ def test_workspace_entry_rejects_bad_workspaces(lib):
 
 
 def test_plan_reports_dynamic_rows(lib):
-    # d = 32768 bf16 on a 152-SM device: one bulk-copy CTA per SM; rows are
-    # taken dynamically (given a workspace) from six rows per CTA on
-    for T, dyn in ((456, 0), (911, 0), (912, 1), (2048, 1)):
-        p = ga.Plan()
-        assert lib.gelu_and_mul_sparse_plan(0x1000, 0x10000000, T, 32768, 65536, ga.BF16, 0, 0,
-                                            152, ctypes.byref(p)) == ga.OK
-        assert p.variant == ga.VARIANT_TMA_ROWS and p.grid == 152
-        assert p.dynamic_rows == dyn, (T, p.dynamic_rows)
+    # d = 16384 bf16 on a 152-SM device: two bulk-copy CTAs per SM from 12
+    # rows per SM on, so six or more per CTA: rows are taken dynamically
+    # (given a workspace)
+    for T, dyn in ((1824, 1), (1825, 1), (4096, 1)):
+        for ws in (0, 1):
+            p = ga.Plan()
+            assert lib.gelu_and_mul_sparse_plan_ex(0x1000, 0x10000000, T, 16384, 32768, ga.BF16,
+                                                   0, 0, 152, ws, ctypes.byref(p)) == ga.OK
+            assert p.variant == ga.VARIANT_TMA_ROWS and p.grid == 304
+            assert p.dynamic_rows == dyn, (T, p.dynamic_rows)
     # a forced bulk-copy geometry always takes rows dynamically; others never
     p = ga.Plan()
     assert lib.gelu_and_mul_sparse_plan(0x1000, 0x10000000, 10, 4096, 8192, ga.BF16,
@@ -263,3 +272,60 @@ def test_plan_reports_dynamic_rows(lib):
     assert lib.gelu_and_mul_sparse_plan(0x1000, 0x10000000, 10, 4096, 8192, ga.BF16,
                                         ga.VARIANT_CTA_ROW, 1, 152, ctypes.byref(p)) == ga.OK
     assert p.dynamic_rows == 0
+
+
+def _plan_ex(lib, T, d, ws, variant=0, cluster=0):
+    p = ga.Plan()
+    rc = lib.gelu_and_mul_sparse_plan_ex(0x1000, 0x10000000, T, d, 2 * d, ga.BF16, variant,
+                                         cluster, 152, ws, ctypes.byref(p))
+    return rc, p
+
+
+def test_plan_pipe_rows_choice(lib):
+    # rows wider than 16384 from ~1.6 rows per SM (d = 32768) on: pipe rows,
+    # one CTA per SM of 16 consumer warps + 1 producer warp, rows always
+    # dynamic given a workspace
+    for T, ws, want in ((200, 1, ga.VARIANT_CTA_ROW), (256, 1, ga.VARIANT_PIPE_ROWS),
+                        (1024, 0, ga.VARIANT_PIPE_ROWS), (1024, 1, ga.VARIANT_PIPE_ROWS),
+                        (2048, 1, ga.VARIANT_PIPE_ROWS), (2048, 0, ga.VARIANT_TMA_ROWS),
+                        (4096, 0, ga.VARIANT_TMA_ROWS)):
+        rc, p = _plan_ex(lib, T, 32768, ws)
+        assert rc == ga.OK and p.variant == want, (T, ws, p.variant)
+        if want == ga.VARIANT_PIPE_ROWS:
+            assert (p.threads, p.vec_per_thread, p.ctas_per_sm, p.grid) == (544, 8, 1, 152)
+            assert p.dynamic_rows == 1 and p.stages == 3
+    # narrower than 32768 but wider than 16384: pipe rows with or without one
+    for d in (20480, 24576):
+        for ws in (0, 1):
+            assert _plan_ex(lib, 2048, d, ws)[1].variant == ga.VARIANT_PIPE_ROWS
+    # d <= 16384 never picks pipe rows by itself
+    for d in (2048, 8192, 16384):
+        for ws in (0, 1):
+            assert _plan_ex(lib, 4096, d, ws)[1].variant != ga.VARIANT_PIPE_ROWS
+
+
+def test_plan_pipe_rows_limits(lib):
+    # every forced setting fits the SM: threads, registers (launch bounds),
+    # shared memory with its per-CTA reserve, three slots or more
+    budget = {4: 4, 8: 2, 16: 1}
+    for d in (64, 1000, 2048, 4096, 8192, 12296, 16384, 24576, 32768):
+        for cps in (0, 1, 2, 4, 8):
+            rc, p = _plan_ex(lib, 4096, d, 1, ga.VARIANT_PIPE_ROWS, cps)
+            if rc != ga.OK:
+                assert rc == ga.ERR_VARIANT
+                continue
+            ncw = p.threads // 32 - 1
+            assert p.variant == ga.VARIANT_PIPE_ROWS and ncw in budget
+            assert p.ctas_per_sm <= budget[ncw] and (cps == 0 or p.ctas_per_sm == cps)
+            assert ncw * 32 * p.vec_per_thread >= d // 8
+            assert p.stages >= 3 and p.ctas_per_sm * (p.smem_bytes + 1024 + 256) <= 228 * 1024
+            assert p.smem_bytes == p.stages * (2 * d + 24)
+        assert _plan_ex(lib, 4096, d, 1, ga.VARIANT_PIPE_ROWS, 0)[0] == ga.OK
+    assert _plan_ex(lib, 4096, 32776, 1, ga.VARIANT_PIPE_ROWS)[0] == ga.ERR_VARIANT
+    assert _plan_ex(lib, 4096, 32768, 1, ga.VARIANT_PIPE_ROWS, 2)[0] == ga.ERR_VARIANT
+    assert _plan_ex(lib, 4096, 64, 1, ga.VARIANT_PIPE_ROWS, 3)[0] == ga.ERR_VARIANT
+    assert _plan_ex(lib, 4096, 64, 1, ga.VARIANT_PIPE_ROWS, 16)[0] == ga.ERR_VARIANT
+    p = ga.Plan()
+    assert lib.gelu_and_mul_sparse_plan_ex(0x1000, 0x100000, 4, 64, 128, ga.F16,
+                                           ga.VARIANT_PIPE_ROWS, 0, 152, 1,
+                                           ctypes.byref(p)) == ga.ERR_VARIANT

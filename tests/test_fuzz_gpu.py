@@ -5,8 +5,9 @@ fp64 oracle with the per-type tolerance of tests/parity.py:
 - the row count, the width and the padding of the rows (NaN-filled);
 - the threshold z (including negative values);
 - the element type;
-- a forced geometry (warp, CTA or cluster rows, scalar, bulk-copy rows with a
-  forced number of CTAs per SM) or the library's own choice;
+- a forced geometry (warp, CTA or cluster rows, scalar, bulk-copy or
+  producer/consumer rows with a forced number of CTAs per SM) or the
+  library's own choice;
 - a workspace (dynamic rows) or none;
 - a constant-gate row, whose output must be exactly zero.
 
@@ -34,8 +35,8 @@ def ga():
     return require_gpu()
 
 
-def draw(i: int) -> dict:
-    r = np.random.default_rng(20_000 + i)
+def draw(i: int, variants=(0, 0, 0, 1, 2, 2, 3, 4, 4), seed0: int = 20_000) -> dict:
+    r = np.random.default_rng(seed0 + i)
     dt = DTYPES[int(r.integers(len(DTYPES)))]
     epv = 16 // ELEM[dt]
     if r.random() < 0.75:                      # the 16-byte layout
@@ -49,12 +50,14 @@ def draw(i: int) -> dict:
     T = int(min(t_max, np.exp(r.uniform(0.0, np.log(4096)))))
     T = max(T, 1)
     z = float(r.choice([0.0, W.Z95, r.uniform(-1.0, 3.0)]))
-    variant = int(r.choice([0, 0, 0, 1, 2, 2, 3, 4, 4]))
+    variant = int(r.choice(list(variants)))
     cluster = 0
     if variant == 2:
         cluster = int(r.choice([0, 1, 2, 4, 8]))
     elif variant == 4:
         cluster = int(r.choice([0, 1, 2, 4, 8, 16]))
+    elif variant == 5:
+        cluster = int(r.choice([0, 0, 1, 2, 4, 8]))
     return {"dtype": dt, "T": T, "d": d, "rs": 2 * d + pad, "z": z, "variant": variant,
             "cluster": cluster, "ws": bool(r.random() < 0.5), "const_row": bool(r.random() < 0.5),
             "seed": 30_000 + i}
@@ -68,13 +71,25 @@ def oracle_result(oracle, x: torch.Tensor, d: int, z: float):
 
 @pytest.mark.parametrize("i", range(N_CASES))
 def test_random_launch(ga, oracle, i):
-    c = draw(i)
+    run_case(ga, oracle, draw(i), f"case {i}")
+
+
+# the producer/consumer geometry, forced (or the library's choice)
+N_PIPE = 80
+
+
+@pytest.mark.parametrize("i", range(N_PIPE))
+def test_random_pipe_launch(ga, oracle, i):
+    run_case(ga, oracle, draw(i, variants=(5, 5, 5, 0), seed0=90_000), f"pipe case {i}")
+
+
+def run_case(ga, oracle, c: dict, name: str):
     T, d, z = c["T"], c["d"], c["z"]
     inp = W.iid(T, d, seed=c["seed"], row_stride=c["rs"], z=z, dtype=c["dtype"])
     x = inp.x.clone()
     if c["const_row"]:
         x[T // 2, :d] = 0.75                   # exact in every element type: std = 0
-    label = f"case {i}: {c}"
+    label = f"{name}: {c}"
     ws = ga.new_workspace() if c["ws"] else None
     try:
         out = ga.gelu_and_mul_sparse(x.cuda(), z, d=d, variant=c["variant"],

@@ -32,7 +32,7 @@ def oracle_of(oracle, x_cpu, d, z):
     return oracle.gelu_and_mul_sparse(W.to_bits(x_cpu.contiguous()), d=d, z=z)
 
 
-GEOMETRIES = [(0, 0), (1, 0), (2, 1), (2, 2), (2, 4), (2, 8), (3, 0), (4, 0)]
+GEOMETRIES = [(0, 0), (1, 0), (2, 1), (2, 2), (2, 4), (2, 8), (3, 0), (4, 0), (5, 0), (5, 1)]
 
 
 @pytest.mark.parametrize("variant,cluster", GEOMETRIES)
@@ -162,7 +162,8 @@ def test_misaligned_input_pointer(ga, oracle, offset):
 
 def test_guard_bands_untouched(ga, oracle):
     for T, d, v in ((4, 2048, 0), (64, 8192, 0), (5, 31, 0), (3, 32768, 0), (2048, 4096, 0),
-                    (2048, 4096, 4), (600, 32768, 4), (7, 2048, 4)):
+                    (2048, 4096, 4), (600, 32768, 4), (7, 2048, 4), (2048, 4096, 5),
+                    (600, 32768, 5), (7, 2048, 5)):
         inp = W.iid(T, d, seed=T + d)
         buf, out = guarded_empty((T, d))
         ga.gelu_and_mul_sparse(inp.x.cuda(), inp.z, out=out, variant=v)

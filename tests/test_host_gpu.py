@@ -46,10 +46,11 @@ def test_gelu_mixed_host_and_device(ga, oracle):
     check_gelu(out_d.cpu(), inp.x, 4096, res, "host in, device out")
 
 
-def test_tma_rows_refuse_host_memory(ga):
+@pytest.mark.parametrize("variant", ["VARIANT_TMA_ROWS", "VARIANT_PIPE_ROWS"])
+def test_bulk_copy_rows_refuse_host_memory(ga, variant):
     x = W.iid(400, 4096, seed=1).x.pin_memory()
     with pytest.raises(ga.GatedActError) as e:
-        ga.gelu_and_mul_sparse(x, W.Z95, variant=ga.VARIANT_TMA_ROWS)
+        ga.gelu_and_mul_sparse(x, W.Z95, variant=getattr(ga, variant))
     assert e.value.status == ga.ERR_VARIANT
 
 

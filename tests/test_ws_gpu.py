@@ -51,17 +51,23 @@ def test_dynamic_rows_match_oracle_and_static_path(ga, oracle, T, d):
     check_gelu(dyn.cpu(), inp.x, d, res, f"dynamic T{T} d{d}")
 
 
-@pytest.mark.parametrize("T,d", [(2048, 16384), (1024, 32768), (1100, 32768)])
-def test_auto_geometry_with_workspace(ga, oracle, T, d):
+# (T, d, geometry with a workspace, same geometry without one)
+@pytest.mark.parametrize("T,d,kind,same", [(2048, 16384, "tma_rows", True),
+                                           (1024, 32768, "pipe_rows", True),
+                                           (1100, 32768, "pipe_rows", True),
+                                           (2048, 32768, "pipe_rows", False)])
+def test_auto_geometry_with_workspace(ga, oracle, T, d, kind, same):
     inp = W.iid(T, d, seed=T + 7 * d)
     x = inp.x.cuda()
-    plan = ga.gelu_and_mul_sparse_plan(x)
-    assert plan["variant"] == "tma_rows" and plan["dynamic_rows"] == 1
+    plan = ga.gelu_and_mul_sparse_plan(x, workspace=True)
+    assert plan["variant"] == kind and plan["dynamic_rows"] == 1
+    assert (ga.gelu_and_mul_sparse_plan(x) == plan) == same
     ws = ga.new_workspace()
     out = ga.gelu_and_mul_sparse(x, inp.z, workspace=ws)
     torch.cuda.synchronize()
     assert _zeroed(ws)
-    assert torch.equal(_bits(out), _bits(ga.gelu_and_mul_sparse(x, inp.z)))
+    if same:   # the same geometry computes every row in the same order
+        assert torch.equal(_bits(out), _bits(ga.gelu_and_mul_sparse(x, inp.z)))
     res = oracle.gelu_and_mul_sparse(W.to_bits(inp.x), d=d, z=inp.z)
     check_gelu(out.cpu(), inp.x, d, res, f"auto+ws T{T} d{d}")
 
