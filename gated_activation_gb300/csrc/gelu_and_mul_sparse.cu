@@ -1130,7 +1130,12 @@ bool pipe_shape_for(int64_t nvec, int cps, int *ncw, int *v, int *stages, int64_
             continue;   // the register budget each kernel is compiled for
         const int64_t chunk = 16 * nvec;
         const int64_t per_cta = std::min<int64_t>(kTmaSmemPerSm / cps, kTmaSmemPerCta) - 1536;
-        const int64_t s = std::min<int64_t>(kPipeMaxStages, per_cta / (chunk + 24));
+        // Ring depth, measured on GB300: about two rows ahead (four slots at
+        // one CTA per SM, five at two) beats a deeper ring, which takes its
+        // rows further ahead and so starts and ends the launch later
+        // (2048 x 16384 at one CTA per SM: 31.3 us with 4 slots, 32.5 with 7).
+        const int64_t depth = cps == 1 ? 4 : cps == 2 ? 5 : kPipeMaxStages;
+        const int64_t s = std::min<int64_t>(depth, per_cta / (chunk + 24));
         if (s < 3)
             continue;
         *ncw = w;
@@ -1150,10 +1155,10 @@ bool pipe_shape(int64_t nvec, int want_cps, int *cps, int *ncw, int *v, int *sta
         *cps = want_cps;
         return pipe_shape_for(nvec, want_cps, ncw, v, stages, smem);
     }
-    // default: as many CTAs per SM as keep 16 KB or more of each row's gate
-    // per CTA in flight: 16384 / d rows' worth
+    // default: as many CTAs per SM as keep the gate half-rows of the rows
+    // in progress on an SM within 32 KB (one CTA per SM from d = 12288 on)
     for (int c = 8; c >= 1; c /= 2) {
-        if (16 * nvec * c > 16 * 2048 * 2 && c > 1)
+        if (16 * nvec * c > 32 * 1024 && c > 1)
             continue;
         if (pipe_shape_for(nvec, c, ncw, v, stages, smem)) {
             *cps = c;
@@ -1251,6 +1256,10 @@ int make_plan(const void *out, const void *in, int64_t T, int64_t d, int64_t rs,
     //    pipe rows; with a workspace (dynamic rows) at any T, without one
     //    while round-robin rows stay below 8 per CTA (d = 32768; beyond that
     //    a slow SM holds the static split back more than in tma rows);
+    //  * d in [14336, 16384]: pipe rows from 8 rows per SM on, with or
+    //    without a workspace (from 6 rows per SM a single launch is faster
+    //    too, but among other activation kernels the switch of the SM's
+    //    shared-memory split around it costs more than it gains);
     //  * tma rows for the widest rows at many rows per SM;
     //  * one CTA per row everywhere else, except a handful of rows of
     //    d >= 16384, where 8-CTA clusters put more SMs on each row.
@@ -1260,6 +1269,8 @@ int make_plan(const void *out, const void *in, int64_t T, int64_t d, int64_t rs,
             variant = GATED_ACT_VARIANT_SCALAR;
         else if (pipe_ok && nvec > 2048 && 10 * T * nvec >= 16 * sm * 4096 &&
                  (has_ws || nvec < 4096 || T < 8 * sm))
+            variant = GATED_ACT_VARIANT_PIPE_ROWS;
+        else if (pipe_ok && nvec >= 1792 && nvec <= 2048 && T >= 8 * sm)
             variant = GATED_ACT_VARIANT_PIPE_ROWS;
         else if (tma_ok && ((nvec >= 4096 && T >= 3 * sm) || (nvec >= 2048 && T >= 12 * sm)))
             variant = GATED_ACT_VARIANT_TMA_ROWS;

@@ -126,12 +126,16 @@ def test_plan_geometry_families(lib):
     for T, d in ((2048, 2048), (2048, 8192), (64, 8192), (1, 4096)):
         rc, p = plan(lib, T, d)
         assert rc == 0 and p["variant"] == "cta_row" and p["cluster"] == 1 and p["grid"] == T
-    # the widest rows at many rows per SM: persistent TMA rows, one wave of CTAs
-    rc, p = plan(lib, 2048, 16384)
-    assert rc == 0 and p["variant"] == "tma_rows" and p["grid"] <= 16 * GB300_SMS
-    assert p["stages"] >= 2 and p["smem_bytes"] <= 227 * 1024
+    # the widest rows at many rows per SM (no workspace): persistent TMA rows,
+    # one wave of CTAs
     rc, p = plan(lib, 2048, 32768)
     assert rc == 0 and p["variant"] == "tma_rows" and p["threads"] == 1024
+    assert p["grid"] == GB300_SMS and p["stages"] >= 2 and p["smem_bytes"] <= 227 * 1024
+    # d = 14336 .. 16384 from 8 rows per SM on: producer/consumer rows, one CTA
+    # per SM of 16 consumer warps, a ring of four slots
+    rc, p = plan(lib, 2048, 16384)
+    assert rc == 0 and p["variant"] == "pipe_rows" and p["threads"] == 544
+    assert p["ctas_per_sm"] == 1 and p["stages"] == 4 and p["grid"] == GB300_SMS
     # rows wider than 16384 at fewer rows per SM: the producer/consumer rows
     rc, p = plan(lib, 512, 32768)
     assert rc == 0 and p["variant"] == "pipe_rows" and p["threads"] == 544
@@ -254,16 +258,20 @@ def test_workspace_entry_rejects_bad_workspaces(lib):
 
 
 def test_plan_reports_dynamic_rows(lib):
-    # d = 16384 bf16 on a 152-SM device: two bulk-copy CTAs per SM from 12
-    # rows per SM on, so six or more per CTA: rows are taken dynamically
-    # (given a workspace)
-    for T, dyn in ((1824, 1), (1825, 1), (4096, 1)):
-        for ws in (0, 1):
-            p = ga.Plan()
-            assert lib.gelu_and_mul_sparse_plan_ex(0x1000, 0x10000000, T, 16384, 32768, ga.BF16,
-                                                   0, 0, 152, ws, ctypes.byref(p)) == ga.OK
-            assert p.variant == ga.VARIANT_TMA_ROWS and p.grid == 304
-            assert p.dynamic_rows == dyn, (T, p.dynamic_rows)
+    # d = 32768 bf16 on a 152-SM device without a workspace: TMA rows from 8
+    # rows per SM on, so eight or more per CTA: rows would be taken
+    # dynamically given a workspace (which picks pipe rows instead)
+    for T in (1216, 2048, 4096):
+        p = ga.Plan()
+        assert lib.gelu_and_mul_sparse_plan_ex(0x1000, 0x10000000, T, 32768, 65536, ga.BF16,
+                                               0, 0, 152, 0, ctypes.byref(p)) == ga.OK
+        assert p.variant == ga.VARIANT_TMA_ROWS and p.grid == 152 and p.dynamic_rows == 1
+    # forced TMA rows below six rows per CTA with a workspace: still dynamic
+    p = ga.Plan()
+    assert lib.gelu_and_mul_sparse_plan_ex(0x1000, 0x10000000, 400, 16384, 32768, ga.BF16,
+                                           ga.VARIANT_TMA_ROWS, 0, 152, 1,
+                                           ctypes.byref(p)) == ga.OK
+    assert p.variant == ga.VARIANT_TMA_ROWS and p.dynamic_rows == 1
     # a forced bulk-copy geometry always takes rows dynamically; others never
     p = ga.Plan()
     assert lib.gelu_and_mul_sparse_plan(0x1000, 0x10000000, 10, 4096, 8192, ga.BF16,
@@ -298,8 +306,18 @@ def test_plan_pipe_rows_choice(lib):
     for d in (20480, 24576):
         for ws in (0, 1):
             assert _plan_ex(lib, 2048, d, ws)[1].variant == ga.VARIANT_PIPE_ROWS
-    # d <= 16384 never picks pipe rows by itself
-    for d in (2048, 8192, 16384):
+    # d = 14336 .. 16384: from 8 rows per SM on, with or without a
+    # workspace; one CTA per SM, four slots
+    for T, d, ws, want in ((1216, 16384, 1, True), (1215, 16384, 1, False),
+                           (1216, 16384, 0, True), (1215, 16384, 0, False),
+                           (2048, 12288, 1, False), (2048, 12288, 0, False),
+                           (2048, 14336, 0, True), (4096, 10240, 1, False)):
+        rc, p = _plan_ex(lib, T, d, ws)
+        assert rc == ga.OK and (p.variant == ga.VARIANT_PIPE_ROWS) == want, (T, d, ws)
+        if want:
+            assert p.ctas_per_sm == 1 and p.stages == 4
+    # d <= 8192 never picks pipe rows by itself
+    for d in (2048, 4096, 8192):
         for ws in (0, 1):
             assert _plan_ex(lib, 4096, d, ws)[1].variant != ga.VARIANT_PIPE_ROWS
 

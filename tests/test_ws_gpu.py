@@ -52,7 +52,7 @@ def test_dynamic_rows_match_oracle_and_static_path(ga, oracle, T, d):
 
 
 # (T, d, geometry with a workspace, same geometry without one)
-@pytest.mark.parametrize("T,d,kind,same", [(2048, 16384, "tma_rows", True),
+@pytest.mark.parametrize("T,d,kind,same", [(2048, 16384, "pipe_rows", True),
                                            (1024, 32768, "pipe_rows", True),
                                            (1100, 32768, "pipe_rows", True),
                                            (2048, 32768, "pipe_rows", False)])
