@@ -144,6 +144,12 @@ def test_plan_geometry_families(lib):
     # a handful of wide rows: 8-CTA clusters per row
     rc, p = plan(lib, 1, 32768)
     assert rc == 0 and p["variant"] == "cta_row" and p["cluster"] == 8
+    # 9 to 32 rows of d >= 32768: 4-CTA clusters
+    for T in (9, 16, 32):
+        rc, p = plan(lib, T, 32768)
+        assert rc == 0 and p["variant"] == "cta_row" and p["cluster"] == 4, T
+    assert plan(lib, 33, 32768)[1]["cluster"] == 1
+    assert plan(lib, 16, 16384)[1]["cluster"] == 1
     # rows wider than one CTA's registers are split across a cluster
     rc, p = plan(lib, 2048, 65536, variant=ga.VARIANT_CTA_ROW)
     assert rc == 0 and p["cluster"] == 2 and p["grid"] == 4096
