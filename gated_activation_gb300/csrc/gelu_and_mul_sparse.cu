@@ -16,13 +16,16 @@
 //                    streaming while earlier rows are reduced and written.
 //                    Rows go round-robin, or, given a workspace, to whichever
 //                    CTA takes the next ticket of an atomic counter;
+//   * pipe rows   -- as tma rows, warp-specialised: one lane of a producer
+//                    warp issues every copy and takes every ticket, the other
+//                    warps finish rows; full/empty mbarriers per slot;
 //   * warp rows   -- one warp per row, shuffles only (d <= 2048);
 //   * CTA row     -- one CTA per row, or a cluster of C CTAs per row, each CTA
-//                    holding a column slice in registers; CTA partials (count,
-//                    sum, M2) are exchanged through distributed shared memory
-//                    and merged with the pairwise update of Chan, Golub and
-//                    LeVeque (1979), so one cluster barrier serves mean and
-//                    variance;
+//                    holding a column slice in registers; in a cluster every
+//                    warp's partials (count, sum, M2) are exchanged through
+//                    distributed shared memory and merged with the update of
+//                    Chan, Golub and LeVeque (1979), so one cluster barrier
+//                    serves mean and variance;
 //   * scalar      -- any alignment or width: 2-byte loads, gate re-read from
 //                    L1/L2 for each pass.
 // The fp32 arithmetic uses Blackwell's paired-lane instructions (add/sub/mul/

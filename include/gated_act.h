@@ -372,9 +372,9 @@ size_t gelu_and_mul_sparse_workspace_bytes(void);
  *              launches sharing one would take each other's row tickets.
  *              The library only reads and writes it from the GPU.
  *   Other arguments as gelu_and_mul_sparse_typed.  Rows are taken
- *   dynamically when the plan's dynamic_rows is 1: the bulk-copy geometry
- *   at six or more rows per CTA, or whenever it is forced; other geometries
- *   ignore the workspace.
+ *   dynamically when the plan's dynamic_rows is 1: pipe rows always, tma
+ *   rows at six or more rows per CTA or whenever they are forced; other
+ *   geometries ignore the workspace.
  * Errors as gelu_and_mul_sparse_typed, plus GATED_ACT_ERR_NULL (no
  * workspace), GATED_ACT_ERR_ALIGN (not 8-byte aligned), GATED_ACT_ERR_OVERLAP
  * (it overlaps in or out) and GATED_ACT_ERR_HOST (host memory).
