@@ -27,8 +27,8 @@
  *     caller and address memory the current device can read and write:
  *     device (or managed) memory, or page-locked host memory (cudaHostAlloc /
  *     cudaHostRegister).  Host buffers are read and written by the kernels in
- *     place, over the CPU-GPU link, with no separate copy (tma_rows is then
- *     not used).  An address the CUDA runtime does not know -- pageable host
+ *     place, over the CPU-GPU link, with no separate copy (the bulk-copy
+ *     geometries, tma rows and pipe rows, are then not used).  An address the CUDA runtime does not know -- pageable host
  *     memory, or no allocation at all -- gives GATED_ACT_ERR_HOST with
  *     nothing launched.  The library
  *     allocates nothing, keeps no state between calls, never synchronizes the
