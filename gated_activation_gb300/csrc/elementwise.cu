@@ -19,7 +19,9 @@
 // run, all loads are issued before any math, and blocks past the live rows
 // are skipped.  VPT = 1 for small launches (more CTAs, so more SMs start
 // loading at once: measured on GB300, silu_and_mul at M = 256..4096, d = 768
-// 3-13% faster), 2 from 2^20 output vectors on (1-3% faster there).  Per element the math is fp32 and independent of the
+// 3-13% faster), 2 from 2^20 output vectors on (1-3% faster there).  The
+// bounded kernel's one wave of CTAs walks blocks of 256 (VPT = 1): 8-25%
+// faster than blocks of 512 at 256..16384 live rows of 16384.  Per element the math is fp32 and independent of the
 // geometry, so any grid (and the scalar path) gives the same bits.
 #include <algorithm>
 
@@ -29,7 +31,8 @@ namespace gact {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kVecPerThread = 2;            // the bounded kernel's blocks
+constexpr int kVecPerThread = 2;            // large unbounded launches
+constexpr int kBoundedVpt = 1;              // the bounded kernel's blocks
 constexpr int64_t kSmallLaunchVectors = int64_t(1) << 20;   // VPT = 1 below
 
 // e^{-|a|} = 2^{-|a| log2 e} on the hardware base-2 exponential (PTX ISA
@@ -157,11 +160,11 @@ ew_vec_bounded(uint16_t *__restrict__ out, const uint16_t *__restrict__ in, int6
                const int32_t *n_rows) {
     pdl_wait();
     pdl_trigger();
-    constexpr int64_t kVecPerCta = int64_t(kThreads) * kVecPerThread;
+    constexpr int64_t kVecPerCta = int64_t(kThreads) * kBoundedVpt;
     const int64_t live = live_rows<true>(M, n_rows);
     for (int64_t first = static_cast<int64_t>(blockIdx.x) * kVecPerCta; first < live * nv;
          first += static_cast<int64_t>(gridDim.x) * kVecPerCta)
-        ew_block<Op, kVecPerThread>(out, in, first, live, nv, in_rs, d, step_r, step_c);
+        ew_block<Op, kBoundedVpt>(out, in, first, live, nv, in_rs, d, step_r, step_c);
 }
 
 // Any layout: one element per thread iteration, 2-byte accesses.
@@ -224,7 +227,7 @@ int run(void *out, const void *in, int64_t M, int64_t d, int64_t in_rs, const in
     cudaError_t e;
     if (vec_ok) {
         const int64_t nv = d / 8;
-        const int vpt = (BOUNDED || M * nv >= kSmallLaunchVectors) ? kVecPerThread : 1;
+        const int vpt = BOUNDED ? kBoundedVpt : M * nv >= kSmallLaunchVectors ? kVecPerThread : 1;
         int64_t grid = ceil_div(M * nv, int64_t(kThreads) * vpt);
         if (BOUNDED)   // one wave: 2048 threads per SM
             grid = std::min<int64_t>(grid, int64_t(device_sm_count()) * (2048 / kThreads));
