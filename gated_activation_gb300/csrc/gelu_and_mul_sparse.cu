@@ -1170,11 +1170,12 @@ struct Plan {
 };
 
 // Threads and vectors per thread for a CTA slice of sv vectors.
-// few_rows (a lone CTA per row, not the native mode, at most two rows per
-// SM): two vectors per thread up to 1024 vectors, so a row spreads over more
-// threads.  Measured on GB300: 7-12% faster at T <= 256 for d = 4096 and
-// 8192 (T = 64, d = 8192: 2.74 against 2.99 us), but 13-23% slower from
-// T = 1024 on, where four vectors per thread let more rows share an SM.
+// few_rows (a lone CTA per row, not the native mode, and the two-vector CTAs
+// of all rows within one wave of 1024 threads per SM): two vectors per thread
+// up to 1024 vectors, so a row spreads over more threads.  Measured on GB300:
+// 6-14% faster at d = 4096 up to T = 608 and at d = 8192 up to T = 304
+// (T = 64, d = 8192: 2.73 against 2.99 us), but 8-23% slower beyond, where
+// four vectors per thread let more rows share an SM.
 void cta_shape(int64_t sv, int *nt, int *v, bool few_rows = false) {
     if (sv <= kMinSliceVec || (few_rows && sv <= 4 * kMinSliceVec)) {
         *v = 2;
@@ -1443,7 +1444,11 @@ int make_plan(const void *out, const void *in, int64_t T, int64_t d, int64_t rs,
         if (sv > kMaxSliceVec)
             return GATED_ACT_ERR_VARIANT;
         int nt, v;
-        cta_shape(sv, &nt, &v, C == 1 && !native && T <= 2 * static_cast<int64_t>(sms));
+        // few rows: the two-vector CTAs of all rows fit in one wave of 1024
+        // threads per SM
+        const bool few_rows =
+            C == 1 && !native && T * pow2_ceil(ceil_div(sv, 2)) <= 1024 * static_cast<int64_t>(sms);
+        cta_shape(sv, &nt, &v, few_rows);
         q.variant = variant;
         q.cluster = C;
         q.threads = nt;
