@@ -24,10 +24,12 @@ def _bits(t):
 
 # (T, d, CTAs per SM; 0 = the library's choice): fewer rows than CTAs, a
 # handful per CTA, many per CTA; widths that fill every consumer vector, and
-# ragged ones (d = 1000: 125 vectors; d = 12296: 1537)
+# ragged ones (d = 1000: 125 vectors; d = 12296: 1537; d = 32760: 4095)
 CASES = [(1, 2048, 0), (7, 4096, 4), (300, 4096, 4), (2000, 1000, 0), (5000, 2048, 4),
          (700, 8192, 2), (2500, 8192, 4), (1300, 8192, 1), (333, 12296, 0), (640, 16384, 2),
-         (2048, 16384, 1), (160, 32768, 1), (3, 32768, 0), (1000, 32768, 1)]
+         (2048, 16384, 1), (160, 32768, 1), (3, 32768, 0), (1000, 32768, 1),
+         # widths between the powers of two, and an odd vector count
+         (300, 20480, 0), (600, 24576, 0), (200, 32760, 0), (257, 16392, 0)]
 
 
 @pytest.mark.parametrize("T,d,cps", CASES)
