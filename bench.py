@@ -728,8 +728,9 @@ def run_e2e_host_direct(args, launches, host_in, world, local, dev) -> dict:
 
 
 # ----------------------------------------------------------------- the oracle on host cores
-def _oracle_pass(o, launches, host_in, rows: int | None) -> int:
-    """Run the fp64 oracle over (the first `rows` rows of) every launch; return bytes."""
+def _oracle_pass(o, launches, host_in, rows: int | None, nthreads: int = 0) -> int:
+    """Run the fp64 oracle over (the first `rows` rows of) every launch on
+    `nthreads` OpenMP threads (0: the default); return bytes."""
     import workloads as W
     done = 0
     for L in launches:
@@ -737,24 +738,62 @@ def _oracle_pass(o, launches, host_in, rows: int | None) -> int:
         r = x.shape[0] if rows is None else min(rows, x.shape[0])
         bits = W.to_bits(x[:r])
         if L["op"] == "gelu":
-            o.gelu_and_mul_sparse(bits, d=L["d"], z=L["z"])
+            o.gelu_and_mul_sparse(bits, d=L["d"], z=L["z"], nthreads=nthreads)
             done += gelu_bytes(r, L["d"])
         else:
-            o.silu_and_mul(bits, d=L["d"])
+            o.silu_and_mul(bits, d=L["d"], nthreads=nthreads)
             done += silu_bytes(r, L["d"])
     return done
 
 
+def cpu_model() -> str:
+    """The host CPU's name, from /proc/cpuinfo where the kernel gives one."""
+    import platform
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read()
+    except OSError:
+        info = ""
+    for key in ("model name", "Model name", "Hardware"):
+        for line in info.splitlines():
+            if line.startswith(key) and ":" in line:
+                return line.split(":", 1)[1].strip()
+    parts = {line.split(":", 1)[0].strip(): line.split(":", 1)[1].strip()
+             for line in info.splitlines() if ":" in line}
+    if "CPU implementer" in parts:   # Arm: implementer and part number
+        return f"{platform.machine()} implementer {parts['CPU implementer']} " \
+               f"part {parts.get('CPU part', '?')}"
+    return platform.machine() or "unknown"
+
+
 def cpu_baseline(launches, host_in) -> dict:
+    """The oracle on the host cores: one full step on every core, and a bounded
+    sample on one core (the first rows of every launch, about 2 s)."""
     import oracle
     o = oracle.default()
+    cores = o.max_threads()
     t0 = time.perf_counter()
     b = _oracle_pass(o, launches, host_in, None)
     dt = time.perf_counter() - t0
-    return {"value": round(b / dt / 1e9, 4), "unit": UNIT, "cores": o.max_threads(),
+    # one core: the first R rows of every launch, R sized from a 1-row pass
+    t1 = time.perf_counter()
+    _oracle_pass(o, launches, host_in, 1, nthreads=1)
+    t1 = max(time.perf_counter() - t1, 1e-4)
+    R = 1
+    while R < 2048 and 2 * R * t1 < 2.0:
+        R *= 2
+    t2 = time.perf_counter()
+    b1 = _oracle_pass(o, launches, host_in, R, nthreads=1)
+    dt1 = time.perf_counter() - t2
+    _oracle_pass(o, launches[:1], host_in, 1, nthreads=cores)   # restore the thread count
+    return {"value": round(b / dt / 1e9, 4), "unit": UNIT, "cores": cores,
             "kind": "oracle",
             "sample": f"one full step of the workload ({len(launches)} launches, {b} algorithmic "
-                      f"bytes) through the fp64 C oracle, OpenMP over rows; {dt:.2f} s wall"}
+                      f"bytes) through the fp64 C oracle, OpenMP over rows; {dt:.2f} s wall",
+            "single_core": {"value": round(b1 / dt1 / 1e9, 4), "unit": UNIT, "cores": 1,
+                            "sample": f"first min(T, {R}) rows of each launch ({b1} algorithmic "
+                                      f"bytes); {dt1:.2f} s wall"},
+            "cpu_model": cpu_model(), "nproc": os.cpu_count()}
 
 
 def run_reference(args, world, rank):
