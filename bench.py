@@ -767,29 +767,32 @@ def cpu_model() -> str:
 
 
 def cpu_baseline(launches, host_in) -> dict:
-    """The oracle on the host cores: one full step on every core, and a bounded
-    sample on one core (the first rows of every launch, about 2 s)."""
+    """The oracle on the host cores: whole steps on every core until about 1 s of
+    wall time (about 16 core-seconds on a 16-core host), and a bounded sample on
+    one core (the first R rows of every launch, R doubled until a pass takes 4 s)."""
     import oracle
     o = oracle.default()
     cores = o.max_threads()
+    passes, b, dt = 0, 0, 0.0
     t0 = time.perf_counter()
-    b = _oracle_pass(o, launches, host_in, None)
-    dt = time.perf_counter() - t0
-    # one core: the first R rows of every launch, R sized from a 1-row pass
-    t1 = time.perf_counter()
-    _oracle_pass(o, launches, host_in, 1, nthreads=1)
-    t1 = max(time.perf_counter() - t1, 1e-4)
-    R = 1
-    while R < 2048 and 2 * R * t1 < 2.0:
+    while passes < 8 and (passes == 0 or dt < 1.0):
+        b += _oracle_pass(o, launches, host_in, None)
+        passes += 1
+        dt = time.perf_counter() - t0
+    R, b1, dt1 = 1, 0, 0.0
+    while True:
+        t1 = time.perf_counter()
+        b1 = _oracle_pass(o, launches, host_in, R, nthreads=1)
+        dt1 = max(time.perf_counter() - t1, 1e-6)
+        if dt1 >= 4.0 or R >= 2048:
+            break
         R *= 2
-    t2 = time.perf_counter()
-    b1 = _oracle_pass(o, launches, host_in, R, nthreads=1)
-    dt1 = time.perf_counter() - t2
     _oracle_pass(o, launches[:1], host_in, 1, nthreads=cores)   # restore the thread count
     return {"value": round(b / dt / 1e9, 4), "unit": UNIT, "cores": cores,
             "kind": "oracle",
-            "sample": f"one full step of the workload ({len(launches)} launches, {b} algorithmic "
-                      f"bytes) through the fp64 C oracle, OpenMP over rows; {dt:.2f} s wall",
+            "sample": f"{passes} full step(s) of the workload ({len(launches)} launches, "
+                      f"{b // passes} algorithmic bytes each) through the fp64 C oracle, "
+                      f"OpenMP over rows; {dt:.2f} s wall",
             "single_core": {"value": round(b1 / dt1 / 1e9, 4), "unit": UNIT, "cores": 1,
                             "sample": f"first min(T, {R}) rows of each launch ({b1} algorithmic "
                                       f"bytes); {dt1:.2f} s wall"},
