@@ -294,6 +294,11 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
 __device__ __forceinline__ void cluster_arrive_release() {
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }
+// Arrive without release: for a CTA whose only claim is that its own reads
+// of its peers' shared memory are done (their values already consumed).
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
 __device__ __forceinline__ void cluster_wait_acquire() {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
@@ -938,7 +943,13 @@ gelu_cta_rows(void *__restrict__ out_, const void *__restrict__ in_, int64_t T, 
                 between = n_l * (dm * dm);
             }
             var = __fdiv_rn(warp_sum(q_l + between), static_cast<float>(d));
-            cluster_arrive_release();   // this CTA is done reading its peers
+            // This CTA is done reading its peers.  No release is needed: the
+            // values read are already consumed, the next exchange barrier (a
+            // release) orders these reads before any peer rewrites this
+            // buffer (double buffering), and this arrive only keeps the
+            // peers resident until the reads are done.  (Measured on GB300:
+            // 3-6% faster than a release arrive for 1-32 rows of d >= 16384.)
+            cluster_arrive_relaxed();
         } else if (!CL) {
             const float s = block_sum<NW>(acc.x + acc.y, red[0], lane, warp);
             mean = __fdiv_rn(s, static_cast<float>(d));
