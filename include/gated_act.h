@@ -386,14 +386,15 @@ int gelu_and_mul_sparse_ws(void *out, const void *in, int64_t T, int64_t d,
 
 /*
  * gelu_and_mul_sparse_ws_static -- gelu_and_mul_sparse_ws for callers that
- * cannot allocate device memory.  The paper has no counterpart to this entry
- * point.  Some callers cannot call cudaMalloc at all: an inference engine
- * that reserved every free byte for its own pool at start-up, or a plugin
- * host that hands a kernel only its inputs and outputs.  For them even a
- * 16-byte workspace is out of reach, and cudaMalloc/cudaFree may also
- * synchronize the device.  This entry point allocates nothing.  Its row
- * counters live in a 256-byte scratch array inside the library, which every
- * GPU that loads the library holds until the process exits.
+ * cannot allocate device memory.  Neither the sparse-GELU page nor the
+ * MoE-activation page defines such an entry point.  Some callers cannot
+ * call cudaMalloc at all: an inference engine that reserved every free byte
+ * for its own pool at start-up, or a plugin host that hands a kernel only
+ * its inputs and outputs.  For them even a 16-byte workspace is out of
+ * reach, and cudaMalloc/cudaFree may also synchronize the device.  This
+ * entry point allocates nothing.  Its row counters live in a 256-byte
+ * scratch array inside the library, which every GPU that loads the library
+ * holds until the process exits.
  *   Arguments as gelu_and_mul_sparse_ws, without the workspace.  The caller
  *   still owns in and out.
  *   The first call on a device looks up the array's device address
