@@ -256,16 +256,29 @@ __device__ __forceinline__ float2 ssd_vec(float2 acc, const uint4 &g, float2 m2)
     return acc;
 }
 
-// CTA-wide sum; every thread returns the same bits.
-template <int NW>
+// CTA-wide sum; every thread returns the same bits.  NARROW: every lane
+// takes the partial of warp (lane mod NW), and a butterfly over NW lanes
+// leaves the total in all 32 lanes (log2 NW shuffles instead of 5).
+// Measured on GB300: 1-6% faster for CTAs of two vectors per thread
+// (decode rows), 2-7% slower for four-vector CTAs, which keep the full tree.
+template <int NW, bool NARROW = false>
 __device__ __forceinline__ float block_sum(float v, float *red, int lane, int warp) {
+    static_assert(NW >= 1 && NW <= 32 && (NW & (NW - 1)) == 0, "warps per CTA: a power of two");
     v = warp_sum(v);
     if (NW == 1)
         return v;
     if (lane == 0)
         red[warp] = v;
     __syncthreads();
-    return warp_sum(lane < NW ? red[lane] : 0.f);
+    if constexpr (NARROW) {
+        float t = red[lane & (NW - 1)];
+#pragma unroll
+        for (int o = NW / 2; o > 0; o >>= 1)
+            t += __shfl_xor_sync(0xFFFFFFFFu, t, o);
+        return t;
+    } else {
+        return warp_sum(lane < NW ? red[lane] : 0.f);
+    }
 }
 
 // Merge statistics (n, sum, M2) of a second group of elements into the first:
@@ -951,7 +964,7 @@ gelu_cta_rows(void *__restrict__ out_, const void *__restrict__ in_, int64_t T, 
             // 3-6% faster than a release arrive for 1-32 rows of d >= 16384.)
             cluster_arrive_relaxed();
         } else if (!CL) {
-            const float s = block_sum<NW>(acc.x + acc.y, red[0], lane, warp);
+            const float s = block_sum<NW, V == 2>(acc.x + acc.y, red[0], lane, warp);
             mean = __fdiv_rn(s, static_cast<float>(d));
             const float2 m2 = make_float2(mean, mean);
             acc = make_float2(0.f, 0.f);
@@ -959,7 +972,7 @@ gelu_cta_rows(void *__restrict__ out_, const void *__restrict__ in_, int64_t T, 
             for (int i = 0; i < V; ++i)
                 if (v0 + tid + NT * i < v1)
                     acc = ssd_vec<F>(acc, g[i], m2);
-            var = __fdiv_rn(block_sum<NW>(acc.x + acc.y, red[1], lane, warp),
+            var = __fdiv_rn(block_sum<NW, V == 2>(acc.x + acc.y, red[1], lane, warp),
                             static_cast<float>(d));
         } else {
             const float s = block_sum<NW>(acc.x + acc.y, red[0], lane, warp);
