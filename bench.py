@@ -395,7 +395,7 @@ def per_shape_times(ga, launches, dev, peak_gbs, reps=5) -> tuple[list, float]:
                "x_floor": round(t / floor, 3), "launches_in_graph": N}
         if "live" in L:
             row["live_rows"] = L["live"]
-        if L["op"] == "gelu" and T <= 64:
+        if L["op"] == "gelu":
             # the same bytes through a purely elementwise kernel (dense
             # gelu_and_mul: no reduction): what streaming these rows costs
             sfns = [lambda x=arena_in[(i % win) * n_in:((i % win) + 1) * n_in].view(T, 2 * d),
