@@ -131,3 +131,64 @@ def test_squared_relu_special_values(ga, oracle):
     # +0 and -0 compare equal
     same = (got == ref16) | (((got | ref16) & 0x7FFF) == 0)
     assert np.all(same | nan)
+
+
+# ------------------------------------------------------------ 2^31-vector launches
+def test_squared_relu_across_the_31_bit_index_boundary(ga, oracle):
+    """Elementwise launches of fewer than 2^31 - 512 16-byte vectors index
+    them in 32 bits, larger ones in 64 bits.  At d = 8 a row is one vector:
+    2^31 - 4096 rows take the 32-bit kernel, 2^31 + 4096 rows the 64-bit one
+    (64 GB of device memory in all).  Four windows of random rows, at the
+    start, on both sides of row 2^31 - 4096 and at the end, are checked bit
+    for bit against the oracle; the other rows are zero, and every output
+    element is written exactly where it should be."""
+    d, W_ = 8, 4096
+    M_big, M_small = (1 << 31) + W_, (1 << 31) - W_
+    free, _ = torch.cuda.mem_get_info()
+    if free < 2 * M_big * d * 2 + (4 << 30):
+        pytest.skip("needs about 68 GB of free device memory")
+    x = out = None
+    try:
+        x = torch.zeros((M_big, d), dtype=torch.bfloat16, device="cuda")
+        out = torch.empty((M_big, d), dtype=torch.bfloat16, device="cuda")
+        o16 = out.view(torch.int16)
+        g = torch.Generator().manual_seed(31)
+        starts = [0, M_small - W_, M_small, M_big - W_]
+        refs = {}
+        for s in starts:
+            v = (3 * torch.randn((W_, d), generator=g)).to(torch.bfloat16)
+            x[s:s + W_] = v.cuda()
+            refs[s] = oracle.squared_relu_rows(W.to_bits(v))[1]
+
+        def window(s):
+            return bits_of(out[s:s + W_])
+
+        def no_sentinel(lo, hi):
+            step = 1 << 27   # rows per chunk: 2 GB of int16 compared at a time
+            for a in range(lo, hi, step):
+                if (o16[a:min(a + step, hi)] == SENTINEL).any().item():
+                    return False
+            return True
+
+        # 32-bit indices: rows [0, M_small) written, the rest untouched
+        o16.fill_(SENTINEL)
+        ga.squared_relu(x[:M_small], out=out[:M_small])
+        torch.cuda.synchronize()
+        assert np.array_equal(window(0), refs[0])
+        assert np.array_equal(window(M_small - W_), refs[M_small - W_])
+        assert bool((o16[M_small:] == SENTINEL).all().item())
+        assert no_sentinel(0, M_small)
+
+        # 64-bit indices: every row written
+        o16.fill_(SENTINEL)
+        ga.squared_relu(x, out=out)
+        torch.cuda.synchronize()
+        for s in starts:
+            assert np.array_equal(window(s), refs[s]), f"rows {s}..{s + W_}"
+        assert no_sentinel(0, M_big)
+        zero_rows = [W_, 1 << 20, (1 << 30) + 12345, M_small - 2 * W_ - 1]
+        for r in zero_rows:
+            assert int((o16[r] != 0).sum().item()) == 0, f"row {r}"
+    finally:
+        del x, out
+        torch.cuda.empty_cache()
