@@ -541,7 +541,8 @@ def run_ours(args, world, rank, local):
                        "launches_per_step": len(launches), "bytes_per_step": bytes_step,
                        "math": "fp32 on bf16 storage",
                        "rows": "gelu launches pass a workspace: the persistent bulk-copy "
-                               "kernel takes rows from an atomic counter at >= 6 rows per CTA",
+                               "kernels take rows from an atomic counter (pipe rows always, "
+                               "tma rows at >= 6 rows per CTA)",
                        "l2": "no flush: every launch has its own buffers (2.6 GB per step, "
                              "129 MB L2), so no launch re-reads data the step touched before",
                        "timing": "per step: graph A (the dominant kernel's launches) then "
@@ -551,6 +552,15 @@ def run_ours(args, world, rank, local):
             "roofline": roofline, "e2e": e2e, "e2e_host_direct": e2e_direct,
             "gpu_launches": len(launches) * args.steps,
             "clocks": clk.summary(), "per_shape": shapes_step, "widened_rows": widened}
+    streamed = [r for r in shapes_step if "stream_us" in r]
+    if streamed:
+        fused = sum(r["us"] for r in streamed)
+        plain = sum(r["stream_us"] for r in streamed)
+        line["vs_stream"] = {
+            "fused_us": round(fused, 1), "stream_us": round(plain, 1),
+            "ratio": round(fused / plain, 3),
+            "what": "sum over the step's gelu shapes of us/launch, fused sparse GELU against "
+                    "the same bytes through the dense gelu_and_mul (no reduction)"}
     if cpu is not None:
         line["cpu_baseline"] = cpu
     if rank == 0:
