@@ -1456,11 +1456,15 @@ int make_plan(const void *out, const void *in, int64_t T, int64_t d, int64_t rs,
                 C *= 2;
             // measured on GB300: 8-CTA clusters for a handful of rows of
             // d >= 16384, 4-CTA clusters for 9-32 rows of d >= 32768
-            // (T = 16: 3.84 against 4.59 us with one CTA per row)
+            // (T = 16: 3.84 against 4.59 us with one CTA per row), 2-CTA
+            // clusters for 33-64 rows of d >= 32768 (T = 64: 5.36 against
+            // 5.54 us; from 96 rows one CTA per row is 10% faster)
             if (T <= kFewRows && nvec >= 2048)
                 C = kMaxCluster;
             else if (T <= 4 * kFewRows && nvec >= 4096)
                 C = std::max(C, 4);
+            else if (T <= 8 * kFewRows && nvec >= 4096)
+                C = std::max(C, 2);
         }
         if (C < 1 || C > kMaxCluster || (C & (C - 1)) != 0)
             return GATED_ACT_ERR_VARIANT;

@@ -148,8 +148,14 @@ def test_plan_geometry_families(lib):
     for T in (9, 16, 32):
         rc, p = plan(lib, T, 32768)
         assert rc == 0 and p["variant"] == "cta_row" and p["cluster"] == 4, T
-    assert plan(lib, 33, 32768)[1]["cluster"] == 1
+    # 33 to 64 rows of d >= 32768: 2-CTA clusters; from 65 rows one CTA per row
+    for T in (33, 48, 64):
+        rc, p = plan(lib, T, 32768)
+        assert rc == 0 and p["variant"] == "cta_row" and p["cluster"] == 2, T
+        assert p["grid"] == 2 * T and p["threads"] == 512
+    assert plan(lib, 65, 32768)[1]["cluster"] == 1
     assert plan(lib, 16, 16384)[1]["cluster"] == 1
+    assert plan(lib, 64, 16384)[1]["cluster"] == 1
     # rows wider than one CTA's registers are split across a cluster
     rc, p = plan(lib, 2048, 65536, variant=ga.VARIANT_CTA_ROW)
     assert rc == 0 and p["cluster"] == 2 and p["grid"] == 4096
