@@ -123,28 +123,104 @@ def ulp_of(c: np.ndarray, dtype: torch.dtype) -> np.ndarray:
     return np.spacing(np.abs(c).astype(np.float32)).astype(np.float64) * 2.0 ** 16
 
 
+def _row_native_failures(y, yb, rb, g, c, nan, expect_nz, dt):
+    """Per-row check of one row against a reference: (zero-pattern mismatches
+    away from the cutoff c, outputs more than one ulp away, flips)."""
+    near = np.abs(g - c) <= ulp_of(np.array([c]), dt)[0]
+    flips = ~nan & ((y != 0) != expect_nz)
+    dist = np.abs(ordered(yb) - ordered(rb))
+    return int((flips & ~near).sum()), int((~nan & ~flips & (dist > 1)).sum()), flips
+
+
+def _adjacent(v: float, dt: torch.dtype, side: int) -> float:
+    """The element-type value next to v (itself of that type) on `side` (+1 up, -1 down)."""
+    b = int(torch.tensor([v], dtype=dt).view(torch.int16).numpy().view(np.uint16)[0])
+    o = int(ordered(np.array([b], dtype=np.uint16))[0]) + side
+    nb = o if o >= 0 else (0x8000 | -o)
+    return float(torch.from_numpy(np.array([nb], dtype=np.uint16).view(np.int16)).view(dt)
+                 .to(torch.float64)[0])
+
+
+def _stat_roundings(v64: float, tol: float, dt: torch.dtype) -> list[float]:
+    """The element-type values a statistic computed in fp32 may round to: the
+    rounding of the exact value v64 (through fp32, as the oracle rounds), and
+    its neighbour across the midpoint when v64 lies within tol of it."""
+    r = float(torch.tensor(v64, dtype=torch.float64).to(torch.float32).to(dt).to(torch.float64))
+    if v64 == r or not np.isfinite(v64):
+        return [r]
+    other = _adjacent(r, dt, 1 if v64 > r else -1)
+    return [r, other] if abs(v64 - 0.5 * (r + other)) <= tol else [r]
+
+
 def check_native(out: torch.Tensor, x: torch.Tensor, d: int, ref: np.ndarray, mask: np.ndarray,
-                 cut: np.ndarray, label: str = "") -> dict:
+                 cut: np.ndarray, label: str = "", z: float | None = None) -> dict:
     """Native-rounding acceptance: outside one rounding step of the row's cutoff
     the zero pattern equals {g > c} exactly; every output is within one
-    element-type ulp of the (already rounded) oracle value."""
+    element-type ulp of the (already rounded) oracle value.
+
+    Several results are correct on a row whose exact mean or population std
+    lies within the fp32 rounding-error bound of recursive summation
+    (2^-24 sum|g| for the mean, 2^-24 (d/2 + 2) std for the std) of a midpoint
+    between two element-type values: the kernel's fp32 statistic may round to
+    either.  Given z, such a row also passes when it meets the same criteria
+    against PyTorch's CPU composition of the native ops with the other
+    rounding (the composition the native oracle reproduces bit for bit)."""
+    import torch.nn.functional as F
     dt = out.dtype
     y = f64_of(out)
     xf = f64_of(x)
     g, u = xf[:, :d], xf[:, d:2 * d]
     nan = np.isnan(ref)
     assert np.array_equal(np.isnan(y), nan), f"{label}: NaN pattern differs"
-    near = np.abs(g - cut[:, None]) <= ulp_of(cut, dt)[:, None]
-    expect_nz = mask & (ref != 0)
-    flips = ~nan & ((y != 0) != expect_nz)
-    bad_mask = flips & ~near
-    assert not bad_mask.any(), f"{label}: {bad_mask.sum()} zero-pattern mismatches away from c"
     yb = out.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
     rb = torch.from_numpy(ref).to(dt).view(torch.int16).numpy().view(np.uint16)
-    dist = np.abs(ordered(yb) - ordered(rb))
-    bad = ~nan & ~flips & (dist > 1)
-    if bad.any():
-        r, c = np.argwhere(bad)[0]
-        raise AssertionError(f"{label}: {bad.sum()} outputs more than 1 ulp away; first ({r},{c}) "
-                             f"out={y[r, c]!r} ref={ref[r, c]!r}")
-    return {"flips_near_cutoff": int(flips.sum()), "ulp1": int((~nan & (dist == 1)).sum())}
+    expect_nz = mask & (ref != 0)
+    n_flips, n_ulp1, n_alt = 0, 0, 0
+    first_bad = None
+    for r in range(y.shape[0]):
+        away, far, flips = _row_native_failures(y[r], yb[r], rb[r], g[r], cut[r], nan[r],
+                                                expect_nz[r], dt)
+        if away == 0 and far == 0:
+            n_flips += int(flips.sum())
+            continue
+        ok = False
+        if z is not None and np.isfinite(g[r]).all():
+            m64 = float(g[r].mean())
+            s64 = float(np.sqrt(((g[r] - m64) ** 2).mean()))
+            ms = _stat_roundings(m64, 2.0 ** -24 * float(np.abs(g[r]).sum()), dt)
+            ss = _stat_roundings(s64, 2.0 ** -24 * (d / 2 + 2) * s64, dt)
+            gt = x[r, :d].detach().cpu()
+            ut = x[r, d:2 * d].detach().cpu()
+            for mv in ms:
+                for sv in ss:
+                    if (mv, sv) == (ms[0], ss[0]):
+                        continue
+                    ct = torch.tensor(mv, dtype=dt) + torch.tensor(sv, dtype=dt) * z
+                    alt = F.gelu(torch.relu(gt - ct), approximate="tanh") * ut
+                    c_alt = float(ct.to(torch.float64))
+                    ab = alt.contiguous().view(torch.int16).numpy().view(np.uint16)
+                    a64 = alt.to(torch.float64).numpy()
+                    a_away, a_far, a_flips = _row_native_failures(
+                        y[r], yb[r], ab, g[r], c_alt, np.isnan(a64), (g[r] > c_alt) & (a64 != 0),
+                        dt)
+                    if a_away == 0 and a_far == 0:
+                        ok = True
+                        n_flips += int(a_flips.sum())
+                        break
+                if ok:
+                    break
+        if ok:
+            n_alt += 1
+            continue
+        if first_bad is None:
+            first_bad = (r, away, far)
+    if first_bad is not None:
+        r, away, far = first_bad
+        if away:
+            raise AssertionError(f"{label}: row {r}: {away} zero-pattern mismatches away from c")
+        dist = np.abs(ordered(yb[r]) - ordered(rb[r]))
+        c = int(np.argmax(dist))
+        raise AssertionError(f"{label}: row {r}: {far} outputs more than 1 ulp away; first "
+                             f"({r},{c}) out={y[r, c]!r} ref={ref[r, c]!r}")
+    n_ulp1 = int((~nan & (np.abs(ordered(yb) - ordered(rb)) == 1)).sum())
+    return {"flips_near_cutoff": n_flips, "ulp1": n_ulp1, "rows_other_rounding": n_alt}

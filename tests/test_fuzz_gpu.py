@@ -136,4 +136,4 @@ def test_random_native_launch(ga, oracle, i):
                                                        bf16_bits=x.dtype == torch.bfloat16)
     out = ga.gelu_and_mul_sparse_native(x.cuda(), z, d=d)
     torch.cuda.synchronize()
-    check_native(out.cpu(), x, d, ref, mask, cut, f"native case {i}: {c}")
+    check_native(out.cpu(), x, d, ref, mask, cut, f"native case {i}: {c}", z=z)

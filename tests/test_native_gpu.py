@@ -38,7 +38,7 @@ def test_native_against_oracle(ga, oracle, dt, z):
                 W.prefill(T=512, dtype=dt), W.sweep(64, 32768, z=z, dtype=dt)):
         ref, mask, cut = oracle_native(oracle, inp.x, inp.d, z)
         check_native(run(ga, inp.x, inp.d, z), inp.x, inp.d, ref, mask, cut,
-                     f"{dt} {inp.name} z{z}")
+                     f"{dt} {inp.name} z{z}", z=z)
 
 
 @pytest.mark.parametrize("dt", DTYPES)
@@ -46,12 +46,12 @@ def test_native_constant_rows_and_ragged(ga, oracle, dt):
     inp = W.sweep(8, 2048, dtype=dt)
     ref, mask, cut = oracle_native(oracle, inp.x, 2048, inp.z)
     out = run(ga, inp.x, 2048, inp.z)
-    check_native(out, inp.x, 2048, ref, mask, cut, f"{dt} const")
+    check_native(out, inp.x, 2048, ref, mask, cut, f"{dt} const", z=inp.z)
     assert torch.count_nonzero(out[-3:].float()).item() == 0
     for T, d, rs in ((5, 31, None), (3, 1, None), (4, 1000, 2048 + 8)):
         inp = W.iid(T, d, seed=d, row_stride=rs, dtype=dt)
         ref, mask, cut = oracle_native(oracle, inp.x, d, inp.z)
-        check_native(run(ga, inp.x, d, inp.z), inp.x, d, ref, mask, cut, f"{dt} d{d}")
+        check_native(run(ga, inp.x, d, inp.z), inp.x, d, ref, mask, cut, f"{dt} d{d}", z=inp.z)
 
 
 @pytest.mark.parametrize("dt", DTYPES)
