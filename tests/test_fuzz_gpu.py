@@ -14,6 +14,8 @@ fp64 oracle with the per-type tolerance of tests/parity.py:
 A forced geometry that does not fit the draw must be refused with
 GATED_ACT_ERR_VARIANT; the library's own choice never is.
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -24,7 +26,9 @@ from tests.parity import check_gelu
 
 pytestmark = pytest.mark.gpu
 
-N_CASES = 200
+# GATED_ACT_FUZZ_SCALE=k runs k times as many draws (the first ones unchanged)
+SCALE = max(1, int(os.environ.get("GATED_ACT_FUZZ_SCALE", "1")))
+N_CASES = 200 * SCALE
 MAX_ELEMS = 3_000_000          # T * d per case, so the oracle stays fast
 DTYPES = (torch.bfloat16, torch.bfloat16, torch.bfloat16, torch.float16, torch.float32)
 ELEM = {torch.bfloat16: 2, torch.float16: 2, torch.float32: 4}
@@ -75,7 +79,7 @@ def test_random_launch(ga, oracle, i):
 
 
 # the producer/consumer geometry, forced (or the library's choice)
-N_PIPE = 80
+N_PIPE = 80 * SCALE
 
 
 @pytest.mark.parametrize("i", range(N_PIPE))
@@ -107,7 +111,7 @@ def run_case(ga, oracle, c: dict, name: str):
 
 
 # ------------------------------------------------------------ native-rounding mode
-N_NATIVE = 60
+N_NATIVE = 60 * SCALE
 
 
 def draw_native(i: int) -> dict:
