@@ -771,8 +771,12 @@ def cpu_model() -> str:
     parts = {line.split(":", 1)[0].strip(): line.split(":", 1)[1].strip()
              for line in info.splitlines() if ":" in line}
     if "CPU implementer" in parts:   # Arm: implementer and part number
-        return f"{platform.machine()} implementer {parts['CPU implementer']} " \
-               f"part {parts.get('CPU part', '?')}"
+        impl, part = parts["CPU implementer"], parts.get("CPU part", "?")
+        # Arm Ltd (0x41) cores by their MIDR part numbers
+        known = {"0xd0c": "Neoverse-N1", "0xd40": "Neoverse-V1", "0xd49": "Neoverse-N2",
+                 "0xd4f": "Neoverse-V2", "0xd8e": "Neoverse-N3", "0xd84": "Neoverse-V3"}
+        name = known.get(part.lower()) if impl.lower() == "0x41" else None
+        return f"{platform.machine()} {name + ' ' if name else ''}(implementer {impl} part {part})"
     return platform.machine() or "unknown"
 
 

@@ -98,3 +98,18 @@ def test_reference_arm_prints_one_json_line():
     assert j["impl"] == "reference" and j["metric"] == bench.METRIC and j["unit"] == "GB/s"
     assert j["value"] > 0 and j["cpu_baseline"]["kind"] == "oracle"
     assert j["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_cpu_model_names_arm_cores(monkeypatch):
+    import builtins
+    import io
+    real_open = builtins.open
+
+    def fake_open(path, *a, **k):
+        if path == "/proc/cpuinfo":
+            return io.StringIO("processor\t: 0\nCPU implementer\t: 0x41\nCPU part\t: 0xd4f\n")
+        return real_open(path, *a, **k)
+
+    monkeypatch.setattr(builtins, "open", fake_open)
+    name = bench.cpu_model()
+    assert "Neoverse-V2" in name and "0xd4f" in name
