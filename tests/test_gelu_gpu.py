@@ -236,3 +236,41 @@ def test_side_stream_and_graph_capture(ga):
     torch.cuda.synchronize()
     for e, o in zip(eager, outs):
         assert torch.equal(e.view(torch.int16), o.view(torch.int16))
+
+
+# rows past 4 GB of input: every row offset needs 64-bit arithmetic
+@pytest.mark.parametrize("T,d,workspace,kind", [
+    (70000, 16384, False, "pipe_rows"),      # 4.6 GB of input
+    (70000, 16384, True, "pipe_rows"),
+    (36001, 32768, False, "tma_rows"),       # 4.7 GB
+    (36001, 32768, True, "pipe_rows"),
+    (140000, 8192, False, "cta_row"),        # 4.6 GB
+])
+def test_rows_past_4gb(ga, oracle, T, d, workspace, kind):
+    """Seven random rows tiled over T rows (T a multiple of 7) on the device:
+    the seven are checked against the oracle, and every other row must equal
+    its source row bit for bit (each row is computed independently by the
+    same code)."""
+    assert T % 7 == 0
+    need = T * 3 * d * 2 + (2 << 30)
+    if torch.cuda.mem_get_info()[0] < need:
+        pytest.skip("not enough free device memory")
+    src = W.iid(7, d, seed=d + 7)
+    res = oracle_of(oracle, src.x, d, src.z)
+    ws = ga.new_workspace() if workspace else None
+    x = out = None
+    try:
+        x = src.x.to("cuda").repeat(T // 7, 1)
+        assert x.numel() * 2 > (1 << 32)
+        assert ga.gelu_and_mul_sparse_plan(x, d=d, workspace=workspace)["variant"] == kind
+        out = ga.gelu_and_mul_sparse(x, src.z, d=d, workspace=ws)
+        torch.cuda.synchronize()
+        check_gelu(out[:7].cpu(), src.x, d, res, f"{T}x{d} rows 0..6")
+        o16 = out.view(torch.int16).view(T // 7, 7, d)
+        same = (o16 == o16[0]).view(T // 7, -1).all(dim=1)
+        assert bool(same.all().item()), f"first differing block {int((~same).nonzero()[0])}"
+        if ws is not None:
+            assert int(ws.count_nonzero().item()) == 0
+    finally:
+        del x, out
+        torch.cuda.empty_cache()
