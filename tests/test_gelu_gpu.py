@@ -80,6 +80,23 @@ def test_sweep(ga, oracle, T, d, z):
     assert torch.count_nonzero(tail).item() == 0
 
 
+@pytest.mark.parametrize("z", W.SWEEP_Z)
+@pytest.mark.parametrize("d", W.SWEEP_D)
+@pytest.mark.parametrize("T", W.SWEEP_T)
+def test_sweep_in_the_bench_configuration(ga, oracle, T, d, z):
+    """The timed launches exactly: T rows (no appended rows), the bench's input
+    (seed 7919 T + d), a workspace, the library's own geometry."""
+    x = W.iid(T, d, seed=W.sweep_seed(T, d), z=z).x
+    res = oracle_of(oracle, x, d, z)
+    ws = ga.new_workspace()
+    xd = x.to("cuda")
+    plan = ga.gelu_and_mul_sparse_plan(xd, d=d, workspace=True)
+    out = ga.gelu_and_mul_sparse(xd, z, d=d, workspace=ws)
+    torch.cuda.synchronize()
+    check_gelu(out.cpu(), x, d, res, f"bench T{T} d{d} z={z} ({plan['variant']})")
+    assert int(ws.count_nonzero().item()) == 0
+
+
 @pytest.mark.parametrize("cluster", [1, 2, 4, 8])
 @pytest.mark.parametrize("T,d", [(8, 8192), (64, 16384), (3, 32768)])
 def test_sweep_shapes_every_cluster(ga, oracle, T, d, cluster):
