@@ -404,6 +404,19 @@ def per_shape_times(ga, launches, dev, peak_gbs, reps=5) -> tuple[list, float]:
             ts = timed_graph(sfns)
             row["stream_us"] = round(ts * 1e3, 3)
             row["x_stream"] = round(t / ts, 3)
+            # a floor this library did not write: device-to-device
+            # cudaMemcpyAsync nodes (torch's copy_ of contiguous bytes) that
+            # read and write half the launch's bytes each, so the same
+            # read + write traffic, from and to the same rotating windows
+            half = L["bytes"] // 2
+            b_in, b_out = arena_in.view(torch.uint8), arena_out.view(torch.uint8)
+            cwin = max(1, min(b_in.numel() // half, b_out.numel() // half))
+            cfns = [lambda s=b_in[(i % cwin) * half:((i % cwin) + 1) * half],
+                    o=b_out[(i % cwin) * half:((i % cwin) + 1) * half]: o.copy_(s)
+                    for i in range(N)]
+            tc = timed_graph(cfns)
+            row["copy_us"] = round(tc * 1e3, 3)
+            row["x_copy"] = round(t / tc, 3)
         rows.append(row)
     del arena_in, arena_out
     torch.cuda.synchronize()
@@ -528,43 +541,105 @@ def run_ours(args, world, rank, local):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(launches, host_in)
 
-    line = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+    full = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": "gelu_and_mul_sparse sweep T{1,8,64,256,1024,2048} x "
-                                   "d{2048,4096,8192,16384,32768} x z{0,1.6448536269514722} "
-                                   "+ silu_and_mul MoE decode M{1024,2048,4096,16384} d768"
-                       if not profiling else (f"gelu_and_mul_sparse T={args.only[0]} d={args.only[1]}"
-                                              if args.only else
-                                              f"silu_and_mul M={args.only_silu} d={launches[0]['d']}"),
+            "config": {"workload": STEP_WORKLOAD if not profiling else
+                       (f"gelu_and_mul_sparse T={args.only[0]} d={args.only[1]}" if args.only else
+                        f"silu_and_mul M={args.only_silu} d={launches[0]['d']}"),
                        "launches_per_step": len(launches), "bytes_per_step": bytes_step,
-                       "math": "fp32 on bf16 storage",
-                       "rows": "gelu launches pass a workspace: the persistent bulk-copy "
-                               "kernels take rows from an atomic counter (pipe rows always, "
-                               "tma rows at >= 6 rows per CTA)",
-                       "l2": "no flush: every launch has its own buffers (2.6 GB per step, "
-                             "129 MB L2), so no launch re-reads data the step touched before",
-                       "timing": "per step: graph A (the dominant kernel's launches) then "
-                                 "graph B (the rest), CUDA events between the two replays",
+                       "l2": "no flush: every launch has its own buffers (2.7 GB per step, "
+                             "129 MB L2)",
                        "parallelism": f"rows sharded over {world} GPU(s), no collective",
                        "launch_floor_us": None if floor_us is None else round(floor_us, 3)},
             "roofline": roofline, "e2e": e2e, "e2e_host_direct": e2e_direct,
             "gpu_launches": len(launches) * args.steps,
             "clocks": clk.summary(), "per_shape": shapes_step, "widened_rows": widened}
-    streamed = [r for r in shapes_step if "stream_us" in r]
-    if streamed:
-        fused = sum(r["us"] for r in streamed)
-        plain = sum(r["stream_us"] for r in streamed)
-        line["vs_stream"] = {
-            "fused_us": round(fused, 1), "stream_us": round(plain, 1),
-            "ratio": round(fused / plain, 3),
-            "what": "sum over the step's gelu shapes of us/launch, fused sparse GELU against "
-                    "the same bytes through the dense gelu_and_mul (no reduction)"}
     if cpu is not None:
-        line["cpu_baseline"] = cpu
+        full["cpu_baseline"] = cpu
     if rank == 0:
-        print(json.dumps(line), flush=True)
+        emit(full, args.detail)
+
+
+STEP_WORKLOAD = ("gelu_and_mul_sparse T{1,8,64,256,1024,2048} x d{2048..32768} x z{0,1.645} "
+                 "+ silu_and_mul M{1024,2048,4096,16384} d768")
+# the shapes north of T*d = 2048*8192 (the bandwidth target) and the decode
+# shapes (d = 8192) that the compact line summarises
+TARGET_SHAPES = ((1024, 16384), (1024, 32768), (2048, 8192), (2048, 16384), (2048, 32768))
+DECODE_SHAPES = ((1, 8192), (8, 8192), (64, 8192))
+LINE_LIMIT = 2000
+
+
+def _shape_row(rows, T, d, z):
+    for r in rows:
+        if r["op"] == "gelu" and r["T"] == T and r["d"] == d and r["z"] == z:
+            return r
+    return None
+
+
+def compact_line(full: dict) -> dict:
+    """The one stdout line: the contract's keys and a short summary of the
+    per-shape table (the full record goes to the --detail file)."""
+    import workloads as W
+    keep = ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+            "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "gpu_launches")
+    line = {k: full[k] for k in keep if k in full}
+    c = full["config"]
+    line["config"] = {k: c[k] for k in ("workload", "bytes_per_step", "l2", "parallelism",
+                                        "launch_floor_us") if k in c}
+    r = full["roofline"]
+    line["roofline"] = {k: r[k] for k in ("bound", "kernel", "achieved", "peak", "unit", "frac",
+                                          "traffic", "avg_launch_us", "peak_source") if k in r}
+    e = full["e2e"]
+    line["e2e"] = {k: e[k] for k in ("value", "unit", "h2d_bytes_per_step",
+                                     "d2h_bytes_per_step", "frac_of_link") if k in e}
+    if "e2e_host_direct" in full:
+        line["e2e"]["host_direct"] = full["e2e_host_direct"]["value"]
+    if "cpu_baseline" in full:
+        cb = full["cpu_baseline"]
+        line["cpu_baseline"] = {"value": cb["value"], "unit": cb["unit"], "cores": cb["cores"],
+                                "kind": cb["kind"], "sample": cb.get("sample_short", cb["sample"]),
+                                "one_core": cb.get("single_core", {}).get("value")}
+    ck = full["clocks"]
+    line["clocks"] = {"sm_mhz": ck.get("sm_mhz"), "sm_max_mhz": ck.get("sm_max_mhz"),
+                      "reasons": ck.get("reasons", [])}
+    rows = full.get("per_shape") or []
+    if rows:
+        # [us, fraction of 8 TB/s, time / device-to-device copy of the same bytes]
+        tg = {}
+        for T, d in TARGET_SHAPES:
+            x = _shape_row(rows, T, d, W.Z95)
+            if x:
+                tg[f"{T}x{d}"] = [x["us"], x["frac_of_spec_8TBps"], x.get("x_copy")]
+        line["targets"] = {"cols": ["us", "of_8TBps", "x_copy"], **tg}
+        # [us, time / (empty launch + bytes at the measured peak), time / copy]
+        dc = {}
+        for T, d in DECODE_SHAPES:
+            x = _shape_row(rows, T, d, W.Z95)
+            if x:
+                dc[f"{T}x{d}"] = [x["us"], x["x_floor"], x.get("x_copy")]
+        line["decode"] = {"cols": ["us", "x_floor", "x_copy"], **dc}
+        gel = [x for x in rows if x["op"] == "gelu" and "copy_us" in x]
+        if gel:
+            fused = sum(x["us"] for x in gel)
+            line["vs_copy"] = round(fused / sum(x["copy_us"] for x in gel), 3)
+            line["vs_stream"] = round(fused / sum(x["stream_us"] for x in gel), 3)
+    line["detail"] = "per-shape and widened-row tables: bench.py --detail FILE"
+    return line
+
+
+def emit(full: dict, detail_path: str | None) -> str:
+    """Write the full record to `detail_path` (if given) and print the compact
+    line, the last line of stdout.  Returns the printed text."""
+    if detail_path:
+        with open(detail_path, "w") as f:
+            json.dump(full, f, indent=1)
+    text = json.dumps(compact_line(full), separators=(",", ":"))
+    if len(text) > LINE_LIMIT:
+        print(f"warning: bench line is {len(text)} bytes", file=sys.stderr)
+    print(text, flush=True)
+    return text
 
 
 def run_e2e(args, launches, host_in, world, local, dev) -> dict:
@@ -810,6 +885,7 @@ def cpu_baseline(launches, host_in) -> dict:
             "single_core": {"value": round(b1 / dt1 / 1e9, 4), "unit": UNIT, "cores": 1,
                             "sample": f"first min(T, {R}) rows of each launch ({b1} algorithmic "
                                       f"bytes); {dt1:.2f} s wall"},
+            "sample_short": f"{passes} whole step(s) on {cores} threads, {dt:.1f} s",
             "cpu_model": cpu_model(), "nproc": os.cpu_count()}
 
 
@@ -866,6 +942,8 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--detail", default=None, metavar="FILE",
+                    help="also write the full record (per-shape and widened-row tables) here")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-shape", action="store_true",
                     help="skip the per-shape us/launch table (profiling runs)")

@@ -32,8 +32,12 @@
 // fma .f32x2), one instruction per two elements.
 #include <algorithm>
 #include <atomic>
+#include <mutex>
+
+#include <cuda.h>
 
 #include "common.cuh"
+#include "gated_act_testing.h"
 
 namespace gact {
 
@@ -1625,14 +1629,19 @@ namespace gact {
 namespace {
 // Validate, resolve host buffers, plan and launch one gelu_and_mul_sparse
 // call.  ws: the caller's workspace (gelu_and_mul_sparse_ws) or nullptr.
+// plan_ws: plan as a call with a workspace even though ws is null (a
+// no-allocation call whose plan takes no rows from a counter).
 int run_gelu(void *out, const void *in, int64_t T, int64_t d, int64_t rs, double z, int dtype,
              int variant, int cluster, bool native, cudaStream_t stream,
-             void *ws = nullptr) {
+             void *ws = nullptr, bool plan_ws = false) {
+    const bool has_ws = ws != nullptr || plan_ws;
     Plan p;
     int rc = make_plan(out, in, T, d, rs, dtype, variant, cluster, 0, true, &p, native, false,
-                       ws != nullptr);
+                       has_ws);
     if (rc != GATED_ACT_OK)
         return rc;
+    if (plan_ws && !ws && p.pub.dynamic_rows)
+        return GATED_ACT_ERR_NULL;   // such a plan needs the counters
     if (ws) {
         if (!aligned(ws, 8))
             return GATED_ACT_ERR_ALIGN;
@@ -1660,7 +1669,7 @@ int run_gelu(void *out, const void *in, int64_t T, int64_t d, int64_t rs, double
         return rc;
     if (hout || hin) {
         rc = make_plan(dout, din, T, d, rs, dtype, variant, cluster, 0, true, &p, native, true,
-                       ws != nullptr);
+                       has_ws);
         if (rc != GATED_ACT_OK)
             return rc;
     }
@@ -1722,23 +1731,80 @@ constexpr size_t kStaticScratchBytes = 256;
 static __device__ __align__(256) unsigned long long g_static_scratch[kStaticScratchBytes / 8];
 
 namespace {
-// Device address of g_static_scratch on the current device, looked up once per
-// device (the first call on a device does it).
+// Unique id of the calling thread's current CUDA context (cuCtxGetId, reached
+// through the runtime's driver entry-point query, so the library links no
+// driver library of its own); 0 when no context is current or the driver
+// cannot tell.  Ids are never reused within a process, so a context made
+// after cudaDeviceReset has a new one.
+unsigned long long current_context_id() {
+    using GetCurrent = CUresult (*)(CUcontext *);
+    using GetId = CUresult (*)(CUcontext, unsigned long long *);
+    struct Fns {
+        GetCurrent cur = nullptr;
+        GetId id = nullptr;
+    };
+    static const Fns fns = [] {
+        Fns f;
+        void *a = nullptr, *b = nullptr;
+        cudaDriverEntryPointQueryResult qa = cudaDriverEntryPointSymbolNotFound, qb = qa;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 12000, cudaEnableDefault,
+                                             &qa) == cudaSuccess &&
+            qa == cudaDriverEntryPointSuccess &&
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &qb) ==
+                cudaSuccess &&
+            qb == cudaDriverEntryPointSuccess) {
+            f.cur = reinterpret_cast<GetCurrent>(a);
+            f.id = reinterpret_cast<GetId>(b);
+        }
+        cudaGetLastError();   // a failed query is not sticky; leave no error behind
+        return f;
+    }();
+    if (!fns.cur || !fns.id)
+        return 0;
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (fns.cur(&ctx) != CUDA_SUCCESS || !ctx || fns.id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
+
+// Device address of g_static_scratch in the current device's current context.
+// A symbol's device address belongs to one context, so the address is looked
+// up once per (device, context): the first call in a context does it, and a
+// new context (after cudaDeviceReset, or a context the caller made current)
+// gets a fresh lookup.  Where the context id is unavailable the address is
+// looked up on every call.
 int static_scratch(void **addr) {
     constexpr int kMaxDevices = 64;
-    static std::atomic<void *> cached[kMaxDevices];
+    struct Entry {
+        unsigned long long ctx;
+        void *ptr;
+    };
+    static Entry cache[kMaxDevices];
+    static std::mutex mu;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return cuda_status(e);
-    void *p = (dev >= 0 && dev < kMaxDevices) ? cached[dev].load(std::memory_order_acquire)
-                                              : nullptr;
-    if (!p) {
-        e = cudaGetSymbolAddress(&p, g_static_scratch);
-        if (e != cudaSuccess)
-            return cuda_status(e);
-        if (dev >= 0 && dev < kMaxDevices)
-            cached[dev].store(p, std::memory_order_release);
+    const bool slot = dev >= 0 && dev < kMaxDevices;
+    unsigned long long ctx = current_context_id();
+    if (slot && ctx != 0) {
+        std::lock_guard<std::mutex> lock(mu);
+        if (cache[dev].ctx == ctx && cache[dev].ptr) {
+            *addr = cache[dev].ptr;
+            return GATED_ACT_OK;
+        }
+    }
+    void *p = nullptr;
+    // makes the device's primary context current if no context is
+    e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess)
+        return cuda_status(e);
+    if (ctx == 0)
+        ctx = current_context_id();
+    if (slot && ctx != 0) {
+        std::lock_guard<std::mutex> lock(mu);
+        cache[dev] = Entry{ctx, p};
     }
     *addr = p;
     return GATED_ACT_OK;
@@ -1758,6 +1824,9 @@ extern "C" int gelu_and_mul_sparse_ws_static(void *out, const void *in, int64_t 
     const size_t need = p.pub.dynamic_rows ? gact::kWorkspaceBytes : 0;
     if (need > gact::kStaticScratchBytes)
         return GATED_ACT_ERR_SCRATCH;
+    if (need == 0)   // the array is neither read nor cleared
+        return gact::run_gelu(out, in, T, d, row_stride, z, dtype, variant, cluster, false,
+                              stream, nullptr, true);
     void *scratch = nullptr;
     if ((rc = gact::static_scratch(&scratch)) != GATED_ACT_OK)
         return rc;

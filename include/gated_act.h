@@ -28,12 +28,17 @@
  *     device (or managed) memory, or page-locked host memory (cudaHostAlloc /
  *     cudaHostRegister).  Host buffers are read and written by the kernels in
  *     place, over the CPU-GPU link, with no separate copy (the bulk-copy
- *     geometries, tma rows and pipe rows, are then not used).  An address the CUDA runtime does not know -- pageable host
- *     memory, or no allocation at all -- gives GATED_ACT_ERR_HOST with
- *     nothing launched.  The library
- *     allocates nothing, keeps no state between calls, never synchronizes the
- *     host and launches only on `stream` (0 = the legacy default stream), so
- *     every call is asynchronous and can be captured in a CUDA graph.
+ *     geometries, tma rows and pipe rows, are then not used).  An address
+ *     the CUDA runtime does not know -- pageable host memory, or no
+ *     allocation at all -- gives GATED_ACT_ERR_HOST with nothing launched.
+ *     The activations allocate no memory, never synchronize the host and
+ *     launch only on `stream` (0 = the legacy default stream), so every call
+ *     is asynchronous and can be captured in a CUDA graph.  The library keeps
+ *     two small pieces of device state per GPU, both in its own static device
+ *     memory: a status word that the bulk-copy kernels set when a bounded
+ *     wait gives up (gated_act_device_status), and the 256-byte scratch array
+ *     of gelu_and_mul_sparse_ws_static.  No other device state outlives a
+ *     call.
  *   - The launch geometry depends only on the arguments, the pointers'
  *     alignment and the device's SM count.
  *   - 16-byte vector paths are taken when `in`, `out`, the row stride and d
@@ -174,50 +179,6 @@ int gated_act_last_cuda_error(void);
  * (it copies a status word), so call it outside stream capture.
  */
 int gated_act_device_status(unsigned int *flags);
-
-/*
- * Exercise the bounded-wait give-up path of the TMA-rows kernel (for tests of
- * the failure handling).  Runs gelu_and_mul_sparse on contiguous [T, 2d] bf16
- * rows with the TMA-rows geometry, except that every CTA withholds the bulk
- * copy of its first row's up half, so the wait for it runs out after wait_ns
- * (0 < wait_ns <= 1e9).  Each CTA then records bit 0 of the device status,
- * waits (bounded) for the copies it did issue and exits: no copy is left in
- * flight and the context stays usable.  Rows a CTA did not finish are left
- * unwritten.  Needs the 16-byte layout and d <= 32768
- * (GATED_ACT_ERR_VARIANT otherwise).
- */
-int gated_act_selftest_wait_timeout(void *out, const void *in, int64_t T,
-                                    int64_t d, unsigned long long wait_ns,
-                                    cudaStream_t stream);
-
-/*
- * gated_act_selftest_wait_timeout with dynamic rows: the same withheld copy
- * per CTA, with rows taken from `workspace` as in gelu_and_mul_sparse_ws
- * (a zeroed device workspace of gelu_and_mul_sparse_workspace_bytes()).
- * A CTA that gives up still draws row tickets until its first failing one,
- * so the launch hands out its usual number and the workspace is left zeroed
- * for the next call.
- */
-int gated_act_selftest_wait_timeout_ws(void *out, const void *in, int64_t T,
-                                       int64_t d, unsigned long long wait_ns,
-                                       void *workspace, cudaStream_t stream);
-
-/*
- * The same self-test for either bulk-copy geometry: variant is
- * GATED_ACT_VARIANT_TMA_ROWS or GATED_ACT_VARIANT_PIPE_ROWS (the library's
- * choice of CTAs per SM); workspace is null (round-robin rows) or a zeroed
- * workspace (dynamic rows).  In the pipe-rows geometry the consumer warps
- * give up on the withheld copy, vote to stop together and leave their slots
- * unreleased; the producer lane sees that, stops issuing, waits (bounded)
- * for the copies it issued that may still be landing, and, with dynamic
- * rows, draws tickets until its first failing one so the workspace is left
- * zeroed.  Errors as gated_act_selftest_wait_timeout_ws, plus
- * GATED_ACT_ERR_VARIANT for any other variant.
- */
-int gated_act_selftest_wait_timeout_ex(void *out, const void *in, int64_t T,
-                                       int64_t d, unsigned long long wait_ns,
-                                       int variant, void *workspace,
-                                       cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
  * Launch-geometry control, for tests and measurements.
@@ -397,14 +358,21 @@ int gelu_and_mul_sparse_ws(void *out, const void *in, int64_t T, int64_t d,
  * holds until the process exits.
  *   Arguments as gelu_and_mul_sparse_ws, without the workspace.  The caller
  *   still owns in and out.
- *   The first call on a device looks up the array's device address
- *   (cudaGetSymbolAddress) with that device current; make that first call
- *   before any stream capture.
- *   Every call shares the one array per device.  Each call first zeroes the
- *   counters on `stream`, then launches.  Calls that overlap on the GPU
- *   (other streams, other threads) race on the counters and can hand rows to
- *   the wrong launch: order such calls on the GPU, or use
- *   gelu_and_mul_sparse_ws with a workspace each.
+ *   Set-up: the array's device address belongs to one CUDA context, so it is
+ *   looked up (cudaGetSymbolAddress) by the first call on a device in each
+ *   context, with that device current, and kept for that context.  A new
+ *   context -- after cudaDeviceReset, or one the caller made current through
+ *   the driver API -- gets its own lookup.  Make the first call on each
+ *   device before any stream capture.
+ *   Only calls whose plan takes rows from a counter use the array
+ *   (gelu_and_mul_sparse_plan_ex with with_workspace = 1 reports
+ *   dynamic_rows = 1): such a call first zeroes the counters on `stream`,
+ *   then launches.  Every such call shares the one array per device, and it
+ *   keeps the last call's contents.  Calls that overlap on the GPU (other
+ *   streams, other threads) race on the counters and can hand rows to the
+ *   wrong launch: order such calls on the GPU, or use gelu_and_mul_sparse_ws
+ *   with a workspace each.  A call whose plan takes no counter neither reads
+ *   nor clears the array.
  *   A call that would need more scratch than the array holds returns
  *   GATED_ACT_ERR_SCRATCH.  This op needs 16 bytes at any size.
  * Results and other errors as gelu_and_mul_sparse_ws.

@@ -14,6 +14,7 @@ from gated_activation_gb300 import build as gbuild
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "gated_act.h")
+TEST_HEADER = os.path.join(ROOT, "include", "gated_act_testing.h")
 GB300_SMS = 152
 
 
@@ -24,10 +25,23 @@ def lib():
     return ga.load_library()
 
 
-def declared_functions() -> list[str]:
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, flags=re.M)))
+def declared_functions(headers=None) -> list[str]:
+    """Functions declared in the given headers (default: every include/*.h)."""
+    if headers is None:
+        inc = os.path.join(ROOT, "include")
+        headers = [os.path.join(inc, f) for f in sorted(os.listdir(inc)) if f.endswith(".h")]
+    names = set()
+    for h in headers:
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names |= set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, flags=re.M))
+    return sorted(names)
+
+
+def test_test_hooks_stay_out_of_the_product_header():
+    product = declared_functions([HEADER])
+    hooks = declared_functions([TEST_HEADER])
+    assert hooks and all("selftest" in n for n in hooks)
+    assert not [n for n in product if "selftest" in n]
 
 
 def test_header_declares_the_boundary():
@@ -40,7 +54,7 @@ def test_header_declares_the_boundary():
 
 def test_library_exports_every_declared_symbol(lib):
     for name in declared_functions():
-        assert hasattr(lib, name), f"{name} declared in gated_act.h but not exported"
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
     assert set(declared_functions()) == set(ga.EXPORTED)
 
 

@@ -113,3 +113,77 @@ def test_cpu_model_names_arm_cores(monkeypatch):
     monkeypatch.setattr(builtins, "open", fake_open)
     name = bench.cpu_model()
     assert "Neoverse-V2" in name and "0xd4f" in name
+
+
+def _synthetic_full_record() -> dict:
+    """A whole-step record shaped like run_ours' (every per-shape and widened
+    row present, long numbers), to size the printed line."""
+    import workloads as W
+    rows = []
+    for L in bench.workload_launches():
+        rows.append({"op": L["op"], "T": L["T"], "d": L["d"], "z": L["z"],
+                     "kernel": "gelu_cta_rows<1024,4,true>", "us": 123.456, "GBps": 6543.2,
+                     "frac_of_measured": 0.9671, "frac_of_spec_8TBps": 0.8179,
+                     "x_floor": 12.345, "launches_in_graph": 200,
+                     **({"stream_us": 121.234, "x_stream": 1.018, "copy_us": 119.876,
+                         "x_copy": 1.029} if L["op"] == "gelu" else {})})
+    widened = [dict(rows[0], op=L["op"]) for L in bench.extra_launches()]
+    return {
+        "metric": bench.METRIC, "value": 4818.3, "unit": "GB/s", "n_gpus": 1, "steps": 200,
+        "warmup": 10, "ms_per_step": 0.56512, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": bench.STEP_WORKLOAD, "launches_per_step": 64,
+                   "bytes_per_step": 2699599872, "l2": "no flush: every launch has its own "
+                   "buffers (2.7 GB per step, 129 MB L2)",
+                   "parallelism": "rows sharded over 1 GPU(s), no collective",
+                   "launch_floor_us": 0.353},
+        "roofline": {"bound": "hbm", "kernel": "gelu_pipe_rows<16,8>", "achieved": 6084.1,
+                     "peak": 6766.0, "unit": "GB/s", "frac": 0.8992, "peak_source": "measured",
+                     "frac_of_spec_8TBps": 0.7605, "launches_per_step": 6,
+                     "bytes_per_launch_avg": 234881024, "avg_launch_us": 35.932,
+                     "time_share": 0.3811, "traffic": 203587211},
+        "e2e": {"value": 270.123, "unit": "GB/s", "ms_per_step": 9.9943, "steps": 10,
+                "reps_ms": [9.9, 10.0, 10.1], "h2d_bytes_per_step": 1799733248,
+                "d2h_bytes_per_step": 899866624, "link_ceiling": 282.1, "frac_of_link": 0.9576,
+                "pipeline": "3 streams", "link": {"value": 282.1}},
+        "e2e_host_direct": {"value": 255.432, "unit": "GB/s", "frac_of_link": 0.8912},
+        "gpu_launches": 12800,
+        "clocks": {"sm_mhz": 2070, "sm_max_mhz": 2070, "reasons": ["sw_power_cap"],
+                   "samples": 123, "source": "nvml"},
+        "per_shape": rows, "widened_rows": widened,
+        "cpu_baseline": {"value": 6.0916, "unit": "GB/s", "cores": 16, "kind": "oracle",
+                         "sample": "3 full step(s) of the workload (64 launches, 2699599872 "
+                                   "algorithmic bytes each) through the fp64 C oracle, OpenMP "
+                                   "over rows; 1.33 s wall",
+                         "sample_short": "3 whole step(s) on 16 threads, 1.3 s",
+                         "single_core": {"value": 0.452, "unit": "GB/s", "cores": 1},
+                         "cpu_model": "aarch64 Neoverse-V2", "nproc": 16},
+        "_z": W.Z95,
+    }
+
+
+def test_bench_line_is_short_and_last(capsys, tmp_path):
+    """The driver keeps only the tail of stdout: the line must be the last one
+    and short enough to survive a tail of a few KB whole."""
+    full = _synthetic_full_record()
+    detail = tmp_path / "detail.json"
+    bench.emit(full, str(detail))
+    out = capsys.readouterr().out
+    last = out.rstrip("\n").splitlines()[-1]
+    assert len(last.encode()) <= 2048, len(last)
+    j = json.loads(last)
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+              "higher_is_better", "dtype", "config", "roofline", "e2e", "cpu_baseline",
+              "gpu_launches", "clocks"):
+        assert k in j, k
+    assert j["config"]["workload"] == bench.STEP_WORKLOAD
+    for k in ("bound", "achieved", "peak", "unit", "frac", "traffic"):
+        assert k in j["roofline"]
+    assert j["e2e"]["h2d_bytes_per_step"] > 0 and j["e2e"]["d2h_bytes_per_step"] > 0
+    for k in ("value", "unit", "cores", "kind", "sample"):
+        assert k in j["cpu_baseline"]
+    assert set(j["targets"]) == {"cols"} | {f"{T}x{d}" for T, d in bench.TARGET_SHAPES}
+    assert set(j["decode"]) == {"cols"} | {f"{T}x{d}" for T, d in bench.DECODE_SHAPES}
+    # the side file keeps every row
+    back = json.loads(detail.read_text())
+    assert len(back["per_shape"]) == 64 and len(back["widened_rows"]) == len(bench.extra_launches())
