@@ -395,15 +395,7 @@ def per_shape_times(ga, launches, dev, peak_gbs, reps=5) -> tuple[list, float]:
                "x_floor": round(t / floor, 3), "launches_in_graph": N}
         if "live" in L:
             row["live_rows"] = L["live"]
-        if L["op"] == "gelu":
-            # the same bytes through a purely elementwise kernel (dense
-            # gelu_and_mul: no reduction): what streaming these rows costs
-            sfns = [lambda x=arena_in[(i % win) * n_in:((i % win) + 1) * n_in].view(T, 2 * d),
-                    o=arena_out[(i % win) * n_out:((i % win) + 1) * n_out].view(T, d):
-                    ga.gelu_and_mul(x, d=d, out=o) for i in range(N)]
-            ts = timed_graph(sfns)
-            row["stream_us"] = round(ts * 1e3, 3)
-            row["x_stream"] = round(t / ts, 3)
+        if L["op"] in ("gelu", "silu"):
             # a floor this library did not write: device-to-device
             # cudaMemcpyAsync nodes (torch's copy_ of contiguous bytes) that
             # read and write half the launch's bytes each, so the same
@@ -417,6 +409,15 @@ def per_shape_times(ga, launches, dev, peak_gbs, reps=5) -> tuple[list, float]:
             tc = timed_graph(cfns)
             row["copy_us"] = round(tc * 1e3, 3)
             row["x_copy"] = round(t / tc, 3)
+        if L["op"] == "gelu":
+            # the same bytes through a purely elementwise kernel (dense
+            # gelu_and_mul: no reduction): what streaming these rows costs
+            sfns = [lambda x=arena_in[(i % win) * n_in:((i % win) + 1) * n_in].view(T, 2 * d),
+                    o=arena_out[(i % win) * n_out:((i % win) + 1) * n_out].view(T, d):
+                    ga.gelu_and_mul(x, d=d, out=o) for i in range(N)]
+            ts = timed_graph(sfns)
+            row["stream_us"] = round(ts * 1e3, 3)
+            row["x_stream"] = round(t / ts, 3)
         rows.append(row)
     del arena_in, arena_out
     torch.cuda.synchronize()
@@ -620,11 +621,19 @@ def compact_line(full: dict) -> dict:
             if x:
                 dc[f"{T}x{d}"] = [x["us"], x["x_floor"], x.get("x_copy")]
         line["decode"] = {"cols": ["us", "x_floor", "x_copy"], **dc}
-        gel = [x for x in rows if x["op"] == "gelu" and "copy_us" in x]
+        sl = {f"{x['T']}": [x["us"], x["x_floor"], x.get("x_copy")]
+              for x in rows if x["op"] == "silu" and x["T"] in (1024, 2048)}
+        if sl:
+            line["silu_d768"] = {"cols": ["us", "x_floor", "x_copy"], **sl}
+        gel = [x for x in rows if x["op"] == "gelu" and "stream_us" in x]
         if gel:
             fused = sum(x["us"] for x in gel)
             line["vs_copy"] = round(fused / sum(x["copy_us"] for x in gel), 3)
             line["vs_stream"] = round(fused / sum(x["stream_us"] for x in gel), 3)
+    nat = [x for x in full.get("widened_rows") or []
+           if x["op"] == "gelu_native" and x["T"] == 2048]
+    if nat:
+        line["native_2048x16384"] = {"us": nat[0]["us"], "frac": nat[0]["frac_of_measured"]}
     line["detail"] = "per-shape and widened-row tables: bench.py --detail FILE"
     return line
 

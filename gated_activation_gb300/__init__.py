@@ -40,7 +40,7 @@ EXPORTED = (
     "silu_and_mul_bounded", "gelu_and_mul",
     "squared_relu", "gelu_and_mul_sparse_workspace_bytes", "gelu_and_mul_sparse_ws",
     "gelu_and_mul_sparse_ws_static", "gated_act_selftest_wait_timeout_ws",
-    "gated_act_selftest_wait_timeout_ex",
+    "gated_act_selftest_wait_timeout_ex", "gelu_and_mul_sparse_native_plan",
 )
 
 
@@ -94,6 +94,9 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
                                                 ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                 ctypes.c_int, ctypes.POINTER(Plan)]
     lib.gelu_and_mul_sparse_plan_ex.restype = ctypes.c_int
+    lib.gelu_and_mul_sparse_native_plan.argtypes = [cvp, cvp, i64, i64, i64, ctypes.c_int,
+                                                    ctypes.c_int, ctypes.POINTER(Plan)]
+    lib.gelu_and_mul_sparse_native_plan.restype = ctypes.c_int
     lib.gelu_and_mul_sparse_typed.argtypes = [vp, cvp, i64, i64, i64, ctypes.c_double,
                                               ctypes.c_int, ctypes.c_int, ctypes.c_int, vp]
     lib.gelu_and_mul_sparse_typed.restype = ctypes.c_int
@@ -272,6 +275,17 @@ def gelu_and_mul_sparse_plan(x: torch.Tensor, d: int | None = None, out: torch.T
     return p.as_dict()
 
 
+def gelu_and_mul_sparse_native_plan(x: torch.Tensor, d: int | None = None) -> dict:
+    """The launch geometry gelu_and_mul_sparse_native would use for ``x``."""
+    T, rs = _rows_view(x, (torch.bfloat16, torch.float16))
+    d = int(x.shape[1]) // 2 if d is None else d
+    p = Plan()
+    rc = load_library().gelu_and_mul_sparse_native_plan(0, x.data_ptr(), T, d, rs,
+                                                        _DTYPE_CODE[x.dtype], 0, ctypes.byref(p))
+    _check("gelu_and_mul_sparse_native_plan", rc)
+    return p.as_dict()
+
+
 def device_status() -> int:
     """Status bits the library's kernels raised on the current device (then cleared).
 
@@ -369,7 +383,7 @@ def squared_relu(x: torch.Tensor, out: torch.Tensor | None = None,
     return out
 
 
-__all__ = ["gelu_and_mul_sparse_native", "silu_and_mul_bounded", "gelu_and_mul", "squared_relu", "gelu_and_mul_sparse", "gelu_and_mul_sparse_plan", "silu_and_mul", "device_status", "noop",
+__all__ = ["gelu_and_mul_sparse_native", "gelu_and_mul_sparse_native_plan", "silu_and_mul_bounded", "gelu_and_mul", "squared_relu", "gelu_and_mul_sparse", "gelu_and_mul_sparse_plan", "silu_and_mul", "device_status", "noop",
            "load_library",
            "status_string", "GatedActError", "Plan", "EXPORTED", "LIB_PATH", "workspace_bytes",
            "new_workspace"]

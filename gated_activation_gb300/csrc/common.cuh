@@ -51,6 +51,15 @@ __device__ __forceinline__ void st_vec(void *p, uint4 v) {
                  : "memory");
 }
 
+// st_vec for an output that nothing else in the kernel reads or writes through
+// another pointer: without the memory clobber the compiler may move other
+// loads (a table read, a shared-memory read) across the store, so the reads
+// of consecutive vectors overlap.  Volatile asm statements keep their order.
+__device__ __forceinline__ void st_vec_out(void *p, uint4 v) {
+    asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};"
+                 :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w));
+}
+
 // Programmatic dependent launch.  Every kernel of the library waits for the
 // preceding grid in its stream to finish (and its memory to be visible)
 // before it touches global memory, and then lets the next PDL-launched grid
@@ -60,6 +69,39 @@ __device__ __forceinline__ void st_vec(void *p, uint4 v) {
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Paired fp32 arithmetic (PTX add/sub/mul/fma .f32x2 on sm_100 and later):
+// one instruction for two lanes, each rounded as its scalar form would be.
+__device__ __forceinline__ unsigned long long u64_of(float2 v) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(v.x), "f"(v.y));
+    return r;
+}
+__device__ __forceinline__ float2 f2_of(unsigned long long r) {
+    float2 v;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
+    return v;
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+    unsigned long long d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(u64_of(a)), "l"(u64_of(b)));
+    return f2_of(d);
+}
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+    unsigned long long d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(u64_of(a)), "l"(u64_of(b)));
+    return f2_of(d);
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+    unsigned long long d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(u64_of(a)), "l"(u64_of(b)));
+    return f2_of(d);
+}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(u64_of(a)), "l"(u64_of(b)), "l"(u64_of(c)));
+    return f2_of(d);
 }
 
 // Butterfly sum: every lane ends with the same bits (fp add is commutative

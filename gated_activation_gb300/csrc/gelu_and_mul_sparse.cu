@@ -68,37 +68,6 @@ constexpr unsigned long long kWaitLimitNs = 1000000000ull;   // 1 s bound on eve
 constexpr int64_t kDynamicRowsPerCta = 6;
 constexpr size_t kWorkspaceBytes = 16;   // a 64-bit row-ticket counter and 8 reserved bytes
 
-// ------------------------------------------------------------ paired fp32 math
-__device__ __forceinline__ unsigned long long u64_of(float2 v) {
-    unsigned long long r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(v.x), "f"(v.y));
-    return r;
-}
-__device__ __forceinline__ float2 f2_of(unsigned long long r) {
-    float2 v;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
-    return v;
-}
-__device__ __forceinline__ float2 add2(float2 a, float2 b) {
-    unsigned long long d;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(u64_of(a)), "l"(u64_of(b)));
-    return f2_of(d);
-}
-__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
-    unsigned long long d;
-    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(u64_of(a)), "l"(u64_of(b)));
-    return f2_of(d);
-}
-__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
-    unsigned long long d;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(u64_of(a)), "l"(u64_of(b)));
-    return f2_of(d);
-}
-__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
-    unsigned long long d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(u64_of(a)), "l"(u64_of(b)), "l"(u64_of(c)));
-    return f2_of(d);
-}
 // max(x, 0) that returns NaN for a NaN input (fmaxf would return 0).
 __device__ __forceinline__ float relu_nan(float x) {
     float y;
@@ -126,7 +95,7 @@ __device__ __forceinline__ float tanh_approx(float x) {
 // in 1 + tanh is below their rounding) and the accurate libm-style tanhf for
 // fp32 outputs.
 struct FmtBf16 {
-    static constexpr int kElem = 2, kPairs = 4;
+    static constexpr int kElem = 2, kPairs = 4, kLut = 0;   // kLut: native table index
     __device__ static float2 pair(const uint4 &v, int i) { return unpack2((&v.x)[i]); }
     __device__ static void put_pair(uint4 &v, int i, float2 f) {
         (&v.x)[i] = pack_bf16x2(f.x, f.y);
@@ -141,7 +110,7 @@ struct FmtBf16 {
 };
 
 struct FmtF16 {
-    static constexpr int kElem = 2, kPairs = 4;
+    static constexpr int kElem = 2, kPairs = 4, kLut = 1;
     __device__ static float2 pair(const uint4 &v, int i) {
         const uint32_t w = (&v.x)[i];
         return __half22float2(*reinterpret_cast<const __half2 *>(&w));
@@ -160,7 +129,7 @@ struct FmtF16 {
 };
 
 struct FmtF32 {
-    static constexpr int kElem = 4, kPairs = 2;
+    static constexpr int kElem = 4, kPairs = 2;   // no native mode, so no kLut
     __device__ static float2 pair(const uint4 &v, int i) {
         return i == 0 ? make_float2(__uint_as_float(v.x), __uint_as_float(v.y))
                       : make_float2(__uint_as_float(v.z), __uint_as_float(v.w));
@@ -211,24 +180,138 @@ template <> __device__ __forceinline__ float round_t<FmtF16>(float x) {
 template <> __device__ __forceinline__ float round_t<FmtF32>(float x) { return x; }
 
 // Native-rounding epilogue: each op of the composition computed in fp32 and
-// rounded to the format -- s = R(g - c), relu, a = R(gelu_tanh(s)) with an
-// accurate tanh, out = R(a * u).
+// rounded to the format -- s = R(g - c), relu, a = R(gelu_tanh(s)), out =
+// R(a * u).  gelu_tanh follows the op order of PyTorch's own tanh-GELU kernel
+// (the composition this mode reproduces): x3 = (s s) s, inner = sqrt(2/pi)
+// fma(0.044715, x3, s), a = (0.5 s)(1 + tanh(inner)), with the accurate
+// tanhf.  a depends only on the 16-bit pattern of s.
 template <class F>
-__device__ __forceinline__ float native_gelu_mul(float g, float u, float c) {
-    const float s = relu_nan(round_t<F>(g - c));
-    const float y = kSqrt2OverPi * (s + 0.044715f * s * s * s);
-    const float a = round_t<F>(0.5f * s * (1.0f + tanhf(y)));
-    return a * u;   // rounded by put_pair
+__device__ __forceinline__ float native_a(float s) {
+    const float x3 = __fmul_rn(__fmul_rn(s, s), s);
+    const float inner = __fmul_rn(kSqrt2OverPi, fmaf(0.044715f, x3, s));
+    return round_t<F>(__fmul_rn(__fmul_rn(0.5f, s), __fadd_rn(1.0f, tanhf(inner))));
 }
 
 template <class F>
-__device__ __forceinline__ uint4 epi_vec_native(const uint4 &g, const uint4 &u, float cutoff) {
+__device__ __forceinline__ float native_gelu_mul(float g, float u, float c) {
+    return native_a<F>(relu_nan(round_t<F>(g - c))) * u;   // rounded by the caller's store
+}
+
+// a = R(gelu_tanh(s)) for every non-negative 16-bit pattern of s, one table
+// per format (64 KB each: [0] bf16, [1] fp16), built once per device by the
+// first native launch that finds it missing (its CTA 0, after which it sets
+// the ready word with release semantics) and read through the read-only cache
+// by later launches.  Entries come from native_a, so a launch that computes a
+// directly (its table not ready yet) gives the same bits.
+__device__ __align__(16) uint16_t g_native_lut[2][32768];
+__device__ unsigned int g_native_lut_ready[2];
+
+template <class F> __device__ __forceinline__ float from_bits(uint32_t p);
+template <> __device__ __forceinline__ float from_bits<FmtBf16>(uint32_t p) {
+    return __uint_as_float(p << 16);
+}
+template <> __device__ __forceinline__ float from_bits<FmtF16>(uint32_t p) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(p)));
+}
+template <class F> __device__ __forceinline__ uint32_t to_bits(float x);
+template <> __device__ __forceinline__ uint32_t to_bits<FmtBf16>(float x) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+template <> __device__ __forceinline__ uint32_t to_bits<FmtF16>(float x) {
+    return __half_as_ushort(__float2half_rn(x));
+}
+
+// R(x.x), R(x.y) packed as the format's 16-bit pair (low element first), and
+// max(pair, 0) on it with NaN kept (the relu of the composition).
+template <class F> __device__ __forceinline__ uint32_t round_pair(float2 x);
+template <> __device__ __forceinline__ uint32_t round_pair<FmtBf16>(float2 x) {
+    return pack_bf16x2(x.x, x.y);
+}
+template <> __device__ __forceinline__ uint32_t round_pair<FmtF16>(float2 x) {
+    const __half2 h = __floats2half2_rn(x.x, x.y);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+template <class F> __device__ __forceinline__ uint32_t relu_pair(uint32_t w);
+template <> __device__ __forceinline__ uint32_t relu_pair<FmtBf16>(uint32_t w) {
+    uint32_t r;
+    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(w), "r"(0u));
+    return r;
+}
+template <> __device__ __forceinline__ uint32_t relu_pair<FmtF16>(uint32_t w) {
+    uint32_t r;
+    asm("max.NaN.f16x2 %0, %1, %2;" : "=r"(r) : "r"(w), "r"(0u));
+    return r;
+}
+
+// Packed products of a format's pairs, each correctly rounded (nearest even).
+template <class F> __device__ __forceinline__ uint32_t mul_pair(uint32_t a, uint32_t b);
+template <> __device__ __forceinline__ uint32_t mul_pair<FmtBf16>(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+template <> __device__ __forceinline__ uint32_t mul_pair<FmtF16>(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// The table of format F, or nullptr while this launch must compute a directly.
+// CTA 0 of a launch that finds the table missing builds it (every thread a
+// strided share), fences, and publishes it; it still computes directly itself,
+// since the read-only cache must not serve data written in the same launch.
+template <class F>
+__device__ const uint16_t *native_table() {
+    __shared__ unsigned int ready;
+    constexpr int k = F::kLut;
+    if (threadIdx.x == 0) {
+        unsigned int v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(&g_native_lut_ready[k])
+                     : "memory");
+        ready = v;
+    }
+    __syncthreads();
+    const unsigned int ok = ready;
+    if (ok)
+        return g_native_lut[k];
+    if (blockIdx.x == 0) {
+        for (uint32_t p = threadIdx.x; p < 32768u; p += blockDim.x)
+            g_native_lut[k][p] = static_cast<uint16_t>(to_bits<F>(native_a<F>(from_bits<F>(p))));
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0)
+            asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(&g_native_lut_ready[k]), "r"(1u)
+                         : "memory");
+    }
+    return nullptr;
+}
+
+// One 16-byte vector of the native epilogue.  With the table: R(g - c) of a
+// pair in one conversion, the relu on the packed pair, two table reads, and
+// R(a u) at the store; without: native_gelu_mul per element.
+template <class F>
+__device__ __forceinline__ uint4 epi_vec_native(const uint4 &g, const uint4 &u, float cutoff,
+                                                const uint16_t *__restrict__ lut) {
     uint4 o;
+    if (lut) {
+        const float2 c2 = make_float2(cutoff, cutoff);
 #pragma unroll
-    for (int i = 0; i < F::kPairs; ++i) {
-        const float2 gp = F::pair(g, i), up = F::pair(u, i);
-        F::put_pair(o, i, make_float2(native_gelu_mul<F>(gp.x, up.x, cutoff),
-                                      native_gelu_mul<F>(gp.y, up.y, cutoff)));
+        for (int i = 0; i < F::kPairs; ++i) {
+            // after the relu both sign bits are clear, so the high index is s >> 16
+            const uint32_t s = relu_pair<F>(round_pair<F>(sub2(F::pair(g, i), c2)));
+            const uint32_t a = static_cast<uint32_t>(__ldg(lut + (s & 0x7FFFu))) |
+                               (static_cast<uint32_t>(__ldg(lut + (s >> 16))) << 16);
+            // R(a u): the product of two 16-bit values is exact in fp32, so
+            // rounding it once is the packed multiply's own rounding
+            (&o.x)[i] = mul_pair<F>(a, (&u.x)[i]);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < F::kPairs; ++i) {
+            const float2 gp = F::pair(g, i), up = F::pair(u, i);
+            F::put_pair(o, i, make_float2(native_gelu_mul<F>(gp.x, up.x, cutoff),
+                                          native_gelu_mul<F>(gp.y, up.y, cutoff)));
+        }
     }
     return o;
 }
@@ -883,6 +966,9 @@ gelu_cta_rows(void *__restrict__ out_, const void *__restrict__ in_, int64_t T, 
     const int64_t rs_bytes = rs * F::kElem, d_bytes = static_cast<int64_t>(d) * F::kElem;
     pdl_wait();
     pdl_trigger();
+    const uint16_t *lut = nullptr;   // native mode: the table of a, once built
+    if constexpr (NATIVE)
+        lut = native_table<F>();
 
     int it = 0;   // rows done by this CTA: the parity picks the exchange buffer
     for (int64_t row = blockIdx.x / C; row < T; row += nclusters, ++it) {
@@ -1020,9 +1106,12 @@ gelu_cta_rows(void *__restrict__ out_, const void *__restrict__ in_, int64_t T, 
 #pragma unroll
         for (int i = 0; i < V; ++i) {
             const int v = v0 + tid + NT * i;
-            if (v < v1)
-                st_vec(op + 16 * v, NATIVE ? epi_vec_native<F>(g[i], u[i], cutoff)
-                                           : epi_vec<F>(g[i], u[i], cutoff));
+            if (v < v1) {
+                if constexpr (NATIVE)
+                    st_vec_out(op + 16 * v, epi_vec_native<F>(g[i], u[i], cutoff, lut));
+                else
+                    st_vec(op + 16 * v, epi_vec<F>(g[i], u[i], cutoff));
+            }
         }
         if (CL)
             cluster_wait_acquire();   // peers are done with xch before it changes
@@ -1100,15 +1189,14 @@ CtaFn cta_fn_t(int nt, int v) {
         switch (nt) {
         case 64: return gelu_cta_rows<64, 2, CL, F, N>;
         case 128: return gelu_cta_rows<128, 2, CL, F, N>;
+        // the few-rows shapes (cta_shape, few_rows): lone CTAs, and CTAs of
+        // 8-CTA clusters
+        case 256: return gelu_cta_rows<256, 2, CL, F, N>;
         default: break;
         }
-        // the few-rows shapes of lone CTAs (cta_shape, few_rows)
-        if constexpr (!CL && !N) {
-            switch (nt) {
-            case 256: return gelu_cta_rows<256, 2, false, F, false>;
-            case 512: return gelu_cta_rows<512, 2, false, F, false>;
-            default: break;
-            }
+        if constexpr (!CL) {
+            if (nt == 512)
+                return gelu_cta_rows<512, 2, false, F, N>;
         }
         return nullptr;
     }
@@ -1198,9 +1286,9 @@ struct Plan {
 };
 
 // Threads and vectors per thread for a CTA slice of sv vectors.
-// few_rows (a lone CTA per row, not the native mode, and the two-vector CTAs
-// of all rows within one wave of 1024 threads per SM): two vectors per thread
-// up to 1024 vectors, so a row spreads over more threads.  Measured on GB300:
+// few_rows (a lone CTA per row, and the two-vector CTAs of all rows within
+// one wave of 1024 threads per SM): two vectors per thread up to 1024
+// vectors, so a row spreads over more threads.  Measured on GB300:
 // 6-14% faster at d = 4096 up to T = 608 and at d = 8192 up to T = 304
 // (T = 64, d = 8192: 2.73 against 2.99 us), but 8-23% slower beyond, where
 // four vectors per thread let more rows share an SM.
@@ -1345,8 +1433,8 @@ int make_plan(const void *out, const void *in, int64_t T, int64_t d, int64_t rs,
     if (variant < GATED_ACT_VARIANT_AUTO || variant > GATED_ACT_VARIANT_PIPE_ROWS)
         return GATED_ACT_ERR_VARIANT;
     const bool forced = variant != GATED_ACT_VARIANT_AUTO;
-    // the warp-rows and TMA-rows kernels exist for plain bf16 only; bulk copies
-    // from host memory are not used
+    // the warp-rows and bulk-copy kernels exist for plain bf16 only; bulk
+    // copies from host memory are not used
     const bool cta_only = dtype != GATED_ACT_BF16 || native;
     const bool bulk = variant == GATED_ACT_VARIANT_TMA_ROWS || variant == GATED_ACT_VARIANT_PIPE_ROWS;
     if (cta_only && (variant == GATED_ACT_VARIANT_WARP_ROWS || bulk))
@@ -1477,9 +1565,12 @@ int make_plan(const void *out, const void *in, int64_t T, int64_t d, int64_t rs,
             return GATED_ACT_ERR_VARIANT;
         int nt, v;
         // few rows: the two-vector CTAs of all rows fit in one wave of 1024
-        // threads per SM
+        // threads per SM; and slices of 8-CTA clusters up to 512 vectors
+        // (d = 32768 at T <= 8: 256 threads of two vectors, measured on
+        // GB300 1-4% faster than 128 threads of four)
         const bool few_rows =
-            C == 1 && !native && T * pow2_ceil(ceil_div(sv, 2)) <= 1024 * static_cast<int64_t>(sms);
+            (C == 1 && T * pow2_ceil(ceil_div(sv, 2)) <= 1024 * static_cast<int64_t>(sms)) ||
+            (C == kMaxCluster && sv <= 2 * kMinSliceVec);
         cta_shape(sv, &nt, &v, few_rows);
         q.variant = variant;
         q.cluster = C;
@@ -1612,6 +1703,27 @@ extern "C" int gelu_and_mul_sparse_plan_ex(const void *out, const void *in, int6
     gact::Plan p;
     const int rc = gact::make_plan(out, in, T, d, row_stride, dtype, variant, cluster, sm_count,
                                    false, &p, false, host, with_workspace != 0);
+    if (rc != GATED_ACT_OK)
+        return rc;
+    *plan = p.pub;
+    return GATED_ACT_OK;
+}
+
+extern "C" int gelu_and_mul_sparse_native_plan(const void *out, const void *in, int64_t T,
+                                               int64_t d, int64_t row_stride, int dtype,
+                                               int sm_count, gated_act_plan *plan) {
+    if (!plan)
+        return GATED_ACT_ERR_NULL;
+    bool host = false;
+    for (const void *q : {out, in}) {
+        const void *dq;
+        bool h = false;
+        if (q && gact::resolve_ptr(q, &dq, &h) == GATED_ACT_OK)
+            host = host || h;
+    }
+    gact::Plan p;
+    const int rc = gact::make_plan(out, in, T, d, row_stride, dtype, GATED_ACT_VARIANT_AUTO, 0,
+                                   sm_count, false, &p, true, host, false);
     if (rc != GATED_ACT_OK)
         return rc;
     *plan = p.pub;

@@ -34,11 +34,11 @@
  *     The activations allocate no memory, never synchronize the host and
  *     launch only on `stream` (0 = the legacy default stream), so every call
  *     is asynchronous and can be captured in a CUDA graph.  The library keeps
- *     two small pieces of device state per GPU, both in its own static device
+ *     three pieces of device state per GPU, all in its own static device
  *     memory: a status word that the bulk-copy kernels set when a bounded
- *     wait gives up (gated_act_device_status), and the 256-byte scratch array
- *     of gelu_and_mul_sparse_ws_static.  No other device state outlives a
- *     call.
+ *     wait gives up (gated_act_device_status), the 256-byte scratch array of
+ *     gelu_and_mul_sparse_ws_static, and the native mode's 64 KB tables (see
+ *     gelu_and_mul_sparse_native).  No other device state outlives a call.
  *   - The launch geometry depends only on the arguments, the pointers'
  *     alignment and the device's SM count.
  *   - 16-byte vector paths are taken when `in`, `out`, the row stride and d
@@ -297,10 +297,27 @@ int gelu_and_mul_sparse_typed(void *out, const void *in, int64_t T, int64_t d,
  * Accuracy: the zero pattern is exactly {g > c}; where the kernel's fp32 row
  * statistics round to the same c as an exact evaluation (all but rare rows),
  * each output is within one element-type ulp of that evaluation.
+ * a = R(gelu_tanh(s)) depends only on the 16-bit pattern of s, so it is
+ * tabulated: the first native launch on a device that finds the table of its
+ * element type missing builds it (32768 entries, 64 KB per type, in the
+ * library's device memory; that launch computes a directly) and later
+ * launches read it through the read-only cache.  Table and direct
+ * evaluation give the same bits.  Rows run one CTA (or cluster) per row,
+ * the geometry with the most L1 for the table.
  */
 int gelu_and_mul_sparse_native(void *out, const void *in, int64_t T, int64_t d,
                                int64_t row_stride, double z, int dtype,
                                cudaStream_t stream);
+
+/*
+ * The launch gelu_and_mul_sparse_native would make, without launching; the
+ * arguments as gelu_and_mul_sparse_plan without the variant, cluster and
+ * workspace (dtype GATED_ACT_BF16 or GATED_ACT_F16; GATED_ACT_ERR_DTYPE
+ * otherwise).
+ */
+int gelu_and_mul_sparse_native_plan(const void *out, const void *in, int64_t T,
+                                    int64_t d, int64_t row_stride, int dtype,
+                                    int sm_count, gated_act_plan *plan);
 
 /* ------------------------------------------------------------------------
  * Dynamic rows through a caller-owned workspace.

@@ -202,6 +202,17 @@ def test_plan_covers_every_slice(lib):
                 pytest.fail(f"aligned d={d} fell back to scalar")
 
 
+def test_plan_eight_cta_clusters_use_two_vector_slices(lib):
+    # a handful of 32768-wide rows: 8-CTA clusters of 256 threads holding two
+    # 16-byte vectors each (512-vector slices)
+    for T in (1, 8):
+        rc, p = plan(lib, T, 32768)
+        assert rc == 0 and p["cluster"] == 8 and p["threads"] == 256 and p["vec_per_thread"] == 2
+    # 4-CTA clusters keep four vectors per thread
+    rc, p = plan(lib, 16, 32768)
+    assert rc == 0 and p["cluster"] == 4 and p["vec_per_thread"] == 4
+
+
 def test_plan_falls_back_to_scalar(lib):
     assert plan(lib, 4, 31)[1]["variant"] == "scalar"            # d not a multiple of 8
     assert plan(lib, 4, 64, rs=130)[1]["variant"] == "scalar"    # row stride not 16-byte
@@ -373,3 +384,23 @@ def test_plan_pipe_rows_limits(lib):
     assert lib.gelu_and_mul_sparse_plan_ex(0x1000, 0x100000, 4, 64, 128, ga.F16,
                                            ga.VARIANT_PIPE_ROWS, 0, 152, 1,
                                            ctypes.byref(p)) == ga.ERR_VARIANT
+
+
+def test_native_plan(lib):
+    # native rows run one CTA (or cluster) per row at every width, where the
+    # plain call streams the widest rows through the bulk-copy kernels
+    p = ga.Plan()
+    for T, d in ((2048, 16384), (1024, 32768), (4096, 64), (1, 32768)):
+        assert lib.gelu_and_mul_sparse_native_plan(0, 0x100000, T, d, 2 * d, ga.BF16,
+                                                   GB300_SMS, ctypes.byref(p)) == 0
+        assert ga.VARIANT_NAMES[p.variant] == "cta_row", (T, d)
+    assert lib.gelu_and_mul_sparse_native_plan(0, 0x100000, 1, 32768, 65536, ga.BF16,
+                                               GB300_SMS, ctypes.byref(p)) == 0
+    assert p.cluster == 8
+    assert lib.gelu_and_mul_sparse_native_plan(0, 0x100000, 2048, 16384, 32768, ga.F16,
+                                               GB300_SMS, ctypes.byref(p)) == 0
+    assert ga.VARIANT_NAMES[p.variant] == "cta_row"
+    assert lib.gelu_and_mul_sparse_native_plan(0, 0x100000, 4, 64, 128, ga.F32, GB300_SMS,
+                                               ctypes.byref(p)) == ga.ERR_DTYPE
+    assert lib.gelu_and_mul_sparse_native_plan(0, 0x100000, 4, 64, 128, ga.BF16, GB300_SMS,
+                                               None) == ga.ERR_NULL

@@ -77,3 +77,50 @@ def test_native_rejects_fp32(ga):
     x = torch.zeros((2, 16), dtype=torch.float32, device="cuda")
     with pytest.raises(TypeError):
         ga.gelu_and_mul_sparse_native(x, 1.0)
+
+
+# bf16 native rows at the widest shapes (one CTA, or two-vector CTAs, per
+# row; the plain call takes the bulk-copy geometries here), against the native
+# oracle
+@pytest.mark.parametrize("T,d,threads", [(2048, 16384, 512), (1300, 14336, 512),
+                                         (1024, 32768, 1024)])
+def test_native_widest_rows(ga, oracle, T, d, threads):
+    inp = W.iid(T, d, seed=T + d)
+    x = inp.x.cuda()
+    plan = ga.gelu_and_mul_sparse_native_plan(x, d=d)
+    assert plan["variant"] == "cta_row" and plan["threads"] == threads, plan
+    ref, mask, cut = oracle_native(oracle, inp.x, d, inp.z)
+    check_native(run(ga, inp.x, d, inp.z), inp.x, d, ref, mask, cut, f"native T{T} d{d}", z=inp.z)
+
+
+_FRESH = r"""
+import sys, torch
+sys.path.insert(0, {root!r})
+import gated_activation_gb300 as ga
+import workloads as W
+torch.cuda.set_device(0)
+res = []
+for dt in (torch.bfloat16, torch.float16):
+    for T, d in ((64, 8192), (2048, 16384)):
+        x = W.iid(T, d, seed=5, dtype=dt).x.cuda()
+        first = ga.gelu_and_mul_sparse_native(x, W.Z95)     # may build the table
+        torch.cuda.synchronize()
+        again = ga.gelu_and_mul_sparse_native(x, W.Z95)     # reads it
+        torch.cuda.synchronize()
+        res.append(bool(torch.equal(first.view(torch.int16), again.view(torch.int16))))
+print("SAME" if all(res) else "DIFF " + str(res))
+"""
+
+
+def test_native_table_and_direct_evaluation_agree_bitwise(ga):
+    """In a fresh process the first native launch finds no table and computes
+    a directly (its CTA 0 builds the table meanwhile); the second reads the
+    table.  The outputs must be identical."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", _FRESH.format(root=root)], capture_output=True,
+                       text=True, timeout=600, cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert r.stdout.strip().endswith("SAME"), r.stdout[-500:]
