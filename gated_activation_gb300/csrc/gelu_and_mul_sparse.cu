@@ -23,9 +23,10 @@
 //   * CTA row     -- one CTA per row, or a cluster of C CTAs per row, each CTA
 //                    holding a column slice in registers; in a cluster every
 //                    warp's partials (count, sum, M2) are exchanged through
-//                    distributed shared memory and merged with the update of
-//                    Chan, Golub and LeVeque (1979), so one cluster barrier
-//                    serves mean and variance;
+//                    distributed shared memory and combined with the
+//                    parallel form of the variance of Chan, Golub and
+//                    LeVeque (1979), M2 = sum M2_p + sum n_p (mean_p -
+//                    mean)^2, so one cluster barrier serves mean and variance;
 //   * scalar      -- any alignment or width: 2-byte loads, gate re-read from
 //                    L1/L2 for each pass.
 // The fp32 arithmetic uses Blackwell's paired-lane instructions (add/sub/mul/
@@ -365,23 +366,6 @@ __device__ __forceinline__ float block_sum(float v, float *red, int lane, int wa
         return t;
     } else {
         return warp_sum(lane < NW ? red[lane] : 0.f);
-    }
-}
-
-// Merge statistics (n, sum, M2) of a second group of elements into the first:
-// the pairwise update of Chan, Golub and LeVeque (1979) written with sums,
-// M2 = M2_a + M2_b + n_a n_b / (n_a + n_b) (mean_b - mean_a)^2.
-__device__ __forceinline__ void merge_stats(float &n, float &s, float &q, float nb, float sb,
-                                            float qb) {
-    if (nb > 0.f) {
-        if (n > 0.f) {
-            const float dm = __fdiv_rn(sb, nb) - __fdiv_rn(s, n);
-            q = q + qb + __fdiv_rn(n * nb, n + nb) * (dm * dm);
-        } else {
-            q = qb;
-        }
-        n += nb;
-        s += sb;
     }
 }
 
@@ -1022,30 +1006,61 @@ gelu_cta_rows(void *__restrict__ out_, const void *__restrict__ in_, int64_t T, 
             }
             cluster_arrive_release();
             cluster_wait_acquire();
-            // lane j takes partial j (CTA j / NW, warp j % NW), and with more
-            // than 32 partials merges j + 32, j + 64, ... into it
-            float n_l = 0.f, s_l = 0.f, q_l = 0.f;
-            if constexpr (kMaxCluster * NW <= 32) {
-                if (lane < C * NW) {
-                    const int k = lane / NW, w = lane - k * NW;
-                    n_l = ld_peer(&x[0][w], k);
-                    s_l = ld_peer(&x[1][w], k);
-                    q_l = ld_peer(&x[2][w], k);
-                }
-            } else {
-                for (int p = lane; p < C * NW; p += 32) {
-                    const int k = p / NW, w = p - k * NW;
-                    merge_stats(n_l, s_l, q_l, ld_peer(&x[0][w], k), ld_peer(&x[1][w], k),
-                                ld_peer(&x[2][w], k));
+            // lane j takes partials j, j + 32, ... (partial p: CTA p / NW,
+            // warp p % NW); M2 = sum_p M2_p + sum_p n_p (mean_p - mean)^2, each
+            // sum a warp reduction over the lanes' shares.  Up to two partials
+            // per lane stay in registers; more are read again after the mean.
+            // (K: the most partials a lane can hold; when the cluster has at
+            // most 32 partials, lane j's single one is also kept.)
+            constexpr int K = (kMaxCluster * NW + 31) / 32;
+            constexpr int KR = K <= 2 ? K : 1;                 // kept in registers
+            const bool one = C * NW <= 32;
+            float n_l[KR], s_l[KR], q_l[KR];
+            float s_sum = 0.f;
+#pragma unroll
+            for (int k = 0; k < K; ++k) {
+                const int p = lane + 32 * k;
+                const bool keep = K <= 2 || k == 0;
+                if (p < C * NW) {
+                    const int c = p / NW, w = p - c * NW;
+                    const float sp = ld_peer(&x[1][w], c);
+                    if (keep) {
+                        n_l[k < KR ? k : 0] = ld_peer(&x[0][w], c);
+                        s_l[k < KR ? k : 0] = sp;
+                        q_l[k < KR ? k : 0] = ld_peer(&x[2][w], c);
+                    }
+                    s_sum += sp;
+                } else if (keep) {
+                    n_l[k < KR ? k : 0] = s_l[k < KR ? k : 0] = q_l[k < KR ? k : 0] = 0.f;
                 }
             }
-            mean = __fdiv_rn(warp_sum(s_l), static_cast<float>(d));
-            float between = 0.f;
-            if (n_l > 0.f) {
-                const float dm = __fdiv_rn(s_l, n_l) - mean;
-                between = n_l * (dm * dm);
+            mean = __fdiv_rn(warp_sum(s_sum), static_cast<float>(d));
+            float q_sum = 0.f;
+#pragma unroll
+            for (int k = 0; k < K; ++k) {
+                float np, sp, qp;
+                if (K <= 2 || k == 0) {
+                    np = n_l[k < KR ? k : 0];
+                    sp = s_l[k < KR ? k : 0];
+                    qp = q_l[k < KR ? k : 0];
+                } else {
+                    if (one)
+                        break;   // every partial was lane j's first
+                    const int p = lane + 32 * k;
+                    np = sp = qp = 0.f;
+                    if (p < C * NW) {
+                        const int c = p / NW, w = p - c * NW;
+                        np = ld_peer(&x[0][w], c);
+                        sp = ld_peer(&x[1][w], c);
+                        qp = ld_peer(&x[2][w], c);
+                    }
+                }
+                if (np > 0.f) {
+                    const float dm = __fdiv_rn(sp, np) - mean;
+                    q_sum += qp + np * (dm * dm);
+                }
             }
-            var = __fdiv_rn(warp_sum(q_l + between), static_cast<float>(d));
+            var = __fdiv_rn(warp_sum(q_sum), static_cast<float>(d));
             // This CTA is done reading its peers.  No release is needed: the
             // values read are already consumed, the next exchange barrier (a
             // release) orders these reads before any peer rewrites this
