@@ -262,7 +262,7 @@ def rank_input(launch: dict, world: int, rank: int):
     """CPU bf16 input of one launch for this rank (rank 0 at N=1: the config's own input)."""
     import workloads as W
     T, d = launch["T"], launch["d"]
-    if launch["op"] == "gelu":
+    if launch["op"] in ("gelu", "gelu_native"):
         seed = W.sweep_seed(T, d) + 1000003 * rank
         return W.iid(T, d, seed=seed, z=launch["z"]).x
     x = W.silu(T, d) if rank == 0 else None
@@ -431,6 +431,9 @@ def run_ours(args, world, rank, local):
     torch.cuda.set_device(local)
     dev = f"cuda:{local}"
     launches = workload_launches(args.only, args.only_silu)
+    if args.native:   # profiling: the same launches in native-rounding mode
+        for L in launches:
+            L["op"] = "gelu_native"
     peaks = load_peaks()
 
     # inputs: seeded on the CPU and copied once to HBM; every launch has its own
@@ -448,6 +451,9 @@ def run_ours(args, world, rank, local):
         if L["op"] == "gelu":
             L["plan"] = ga.gelu_and_mul_sparse_plan(dev_in[i], d=L["d"], workspace=True)
             L["kernel"] = kernel_name(L["plan"])
+        elif L["op"] == "gelu_native":
+            L["plan"] = ga.gelu_and_mul_sparse_native_plan(dev_in[i], d=L["d"])
+            L["kernel"] = kernel_name(L["plan"]) + " native"
         else:
             L["plan"] = None
             L["kernel"] = "silu_vec"
@@ -831,7 +837,7 @@ def _oracle_pass(o, launches, host_in, rows: int | None, nthreads: int = 0) -> i
         x = host_in[L["key"]]
         r = x.shape[0] if rows is None else min(rows, x.shape[0])
         bits = W.to_bits(x[:r])
-        if L["op"] == "gelu":
+        if L["op"] in ("gelu", "gelu_native"):
             o.gelu_and_mul_sparse(bits, d=L["d"], z=L["z"], nthreads=nthreads)
             done += gelu_bytes(r, L["d"])
         else:
@@ -959,11 +965,15 @@ def parse_args(argv=None):
     ap.add_argument("--only", type=lambda s: tuple(float(v) if "." in v else int(v)
                                                    for v in s.split(",")), default=None,
                     help="time one gelu shape T,d[,z] (profiling); not a bench line")
+    ap.add_argument("--native", action="store_true",
+                    help="with --only: the launches in native-rounding mode (profiling)")
     ap.add_argument("--only-silu", type=int, default=None, metavar="M",
                     help="time one silu_and_mul row count M (profiling); not a bench line")
     a = ap.parse_args(argv)
     if a.warmup < 3 and a.impl == "ours":
         ap.error("--warmup must be >= 3")
+    if a.native and not a.only:
+        ap.error("--native needs --only T,d")
     return a
 
 
