@@ -261,13 +261,20 @@ template <> __device__ __forceinline__ uint32_t mul_pair<FmtF16>(uint32_t a, uin
 // CTA 0 of a launch that finds the table missing builds it (every thread a
 // strided share), fences, and publishes it; it still computes directly itself,
 // since the read-only cache must not serve data written in the same launch.
+// The ready word is read relaxed, not with acquire: the table is written once,
+// every writer fences, and the word is published with a release store after
+// that; a reader issues its table reads (read-only path) only after the word's
+// value has decided its branch, and no SM holds earlier copies of table lines
+// (nothing reads the table before it is published).  An acquire at GPU scope
+// would also invalidate the SM's L1 at every CTA start, evicting the table's
+// hot lines: measured on GB300, 1.5% slower at 2048 x 16384.
 template <class F>
 __device__ const uint16_t *native_table() {
     __shared__ unsigned int ready;
     constexpr int k = F::kLut;
     if (threadIdx.x == 0) {
         unsigned int v;
-        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(&g_native_lut_ready[k])
+        asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(&g_native_lut_ready[k])
                      : "memory");
         ready = v;
     }
