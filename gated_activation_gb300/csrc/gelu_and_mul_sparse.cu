@@ -32,7 +32,6 @@
 // The fp32 arithmetic uses Blackwell's paired-lane instructions (add/sub/mul/
 // fma .f32x2), one instruction per two elements.
 #include <algorithm>
-#include <atomic>
 #include <mutex>
 
 #include <cuda.h>
@@ -1615,18 +1614,68 @@ int make_plan(const void *out, const void *in, int64_t T, int64_t d, int64_t rs,
     return GATED_ACT_OK;
 }
 
-// Shared memory above 48 KB needs a per-kernel opt-in, done once per device;
-// the carveout hint asks for the largest shared-memory split of L1.
+// Unique id of the calling thread's current CUDA context (cuCtxGetId, reached
+// through the runtime's driver entry-point query, so the library links no
+// driver library of its own); 0 when no context is current or the driver
+// cannot tell.  Ids are never reused within a process, so a context made
+// after cudaDeviceReset has a new one.
+unsigned long long current_context_id() {
+    using GetCurrent = CUresult (*)(CUcontext *);
+    using GetId = CUresult (*)(CUcontext, unsigned long long *);
+    struct Fns {
+        GetCurrent cur = nullptr;
+        GetId id = nullptr;
+    };
+    static const Fns fns = [] {
+        Fns f;
+        void *a = nullptr, *b = nullptr;
+        cudaDriverEntryPointQueryResult qa = cudaDriverEntryPointSymbolNotFound, qb = qa;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 12000, cudaEnableDefault,
+                                             &qa) == cudaSuccess &&
+            qa == cudaDriverEntryPointSuccess &&
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &qb) ==
+                cudaSuccess &&
+            qb == cudaDriverEntryPointSuccess) {
+            f.cur = reinterpret_cast<GetCurrent>(a);
+            f.id = reinterpret_cast<GetId>(b);
+        }
+        cudaGetLastError();   // a failed query is not sticky; leave no error behind
+        return f;
+    }();
+    if (!fns.cur || !fns.id)
+        return 0;
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (fns.cur(&ctx) != CUDA_SUCCESS || !ctx || fns.id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
+
+// Shared memory above 48 KB needs a per-kernel opt-in; the carveout hint asks
+// for the largest shared-memory split of L1.  Both are attributes of the
+// kernel in one context, so they are set once per (device, context): a new
+// context (after cudaDeviceReset, or one the caller made current) sets them
+// again, and where the context id is unavailable they are set on every call.
 // key: a bit index in [0, 32) that names the kernel.
 int ensure_smem_attr(TmaFn fn, int key) {
     constexpr int kMaxDevices = 64;
-    static std::atomic<unsigned> done[kMaxDevices];
+    struct Entry {
+        unsigned long long ctx;
+        unsigned bits;
+    };
+    static Entry done[kMaxDevices];
+    static std::mutex mu;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess)
         dev = -1;
+    const bool slot = dev >= 0 && dev < kMaxDevices;
     const unsigned bit = 1u << key;
-    if (dev >= 0 && dev < kMaxDevices && (done[dev].load(std::memory_order_acquire) & bit))
-        return GATED_ACT_OK;
+    const unsigned long long ctx = slot ? current_context_id() : 0;
+    if (ctx != 0) {
+        std::lock_guard<std::mutex> lock(mu);
+        if (done[dev].ctx == ctx && (done[dev].bits & bit))
+            return GATED_ACT_OK;
+    }
     cudaFuncAttributes fa;
     cudaError_t e = cudaFuncGetAttributes(&fa, fn);
     if (e == cudaSuccess)
@@ -1637,8 +1686,12 @@ int ensure_smem_attr(TmaFn fn, int key) {
                                  cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess)
         return cuda_status(e);
-    if (dev >= 0 && dev < kMaxDevices)
-        done[dev].fetch_or(bit, std::memory_order_acq_rel);
+    if (ctx != 0) {
+        std::lock_guard<std::mutex> lock(mu);
+        if (done[dev].ctx != ctx)
+            done[dev] = Entry{ctx, 0u};
+        done[dev].bits |= bit;
+    }
     return GATED_ACT_OK;
 }
 
@@ -1865,43 +1918,6 @@ constexpr size_t kStaticScratchBytes = 256;
 static __device__ __align__(256) unsigned long long g_static_scratch[kStaticScratchBytes / 8];
 
 namespace {
-// Unique id of the calling thread's current CUDA context (cuCtxGetId, reached
-// through the runtime's driver entry-point query, so the library links no
-// driver library of its own); 0 when no context is current or the driver
-// cannot tell.  Ids are never reused within a process, so a context made
-// after cudaDeviceReset has a new one.
-unsigned long long current_context_id() {
-    using GetCurrent = CUresult (*)(CUcontext *);
-    using GetId = CUresult (*)(CUcontext, unsigned long long *);
-    struct Fns {
-        GetCurrent cur = nullptr;
-        GetId id = nullptr;
-    };
-    static const Fns fns = [] {
-        Fns f;
-        void *a = nullptr, *b = nullptr;
-        cudaDriverEntryPointQueryResult qa = cudaDriverEntryPointSymbolNotFound, qb = qa;
-        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 12000, cudaEnableDefault,
-                                             &qa) == cudaSuccess &&
-            qa == cudaDriverEntryPointSuccess &&
-            cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &qb) ==
-                cudaSuccess &&
-            qb == cudaDriverEntryPointSuccess) {
-            f.cur = reinterpret_cast<GetCurrent>(a);
-            f.id = reinterpret_cast<GetId>(b);
-        }
-        cudaGetLastError();   // a failed query is not sticky; leave no error behind
-        return f;
-    }();
-    if (!fns.cur || !fns.id)
-        return 0;
-    CUcontext ctx = nullptr;
-    unsigned long long id = 0;
-    if (fns.cur(&ctx) != CUDA_SUCCESS || !ctx || fns.id(ctx, &id) != CUDA_SUCCESS)
-        return 0;
-    return id;
-}
-
 // Device address of g_static_scratch in the current device's current context.
 // A symbol's device address belongs to one context, so the address is looked
 // up once per (device, context): the first call in a context does it, and a
