@@ -38,20 +38,27 @@ constexpr int kVecPerThread = 2;            // large unbounded launches
 constexpr int kBoundedVpt = 1;              // the bounded kernel's blocks
 constexpr int64_t kSmallLaunchVectors = int64_t(1) << 20;   // VPT = 1 below
 
-// e^{-|a|} = 2^{-|a| log2 e} on the hardware base-2 exponential (PTX ISA
-// ex2.approx.f32, the non-flushing form: subnormal results survive).
+// e^{-|a|} as the square of h = e^{-|a|/2} = 2^{-|a| log2(e) / 2} (PTX ISA
+// ex2.approx.ftz.f32, one special-function instruction).  h is a normal
+// number for |a| < 174 (2^-126 at |a| = 174.7), where the flushing form of
+// the exponential is exact to its approximation; the product h * h (an
+// ordinary multiply, which keeps subnormals) carries e^{-|a|} down to the
+// subnormal results that a product silu(a) * u of ordinary size can still
+// need.  Beyond |a| = 174, e^{-|a|} < 2^-251 and every result that uses it
+// rounds to zero in bf16 as it does in fp32.
 __device__ __forceinline__ float exp_neg_abs(float a) {
-    const float x = -fabsf(a) * 1.4426950408889634f;
-    float y;
-    asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
+    const float x = fabsf(a) * (-0.5f * 1.4426950408889634f);
+    float h;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(h) : "f"(x));
+    return h * h;
 }
 
-// 1 + t lies in (1, 2], where the hardware reciprocal (PTX ISA rcp.approx.f32)
-// is within one fp32 ulp; the bf16 result tolerates far more.
+// 1 + t lies in [1, 2], where the flushing form of the hardware reciprocal
+// (PTX ISA rcp.approx.ftz.f32, one special-function instruction) is within
+// one fp32 ulp: no subnormal input or result can occur.
 __device__ __forceinline__ float rcp_approx(float x) {
     float y;
-    asm("rcp.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
 
