@@ -22,7 +22,7 @@ LIB_PATH = _build.LIB
 OK = 0
 ERR_NULL, ERR_SIZE, ERR_STRIDE, ERR_TOO_LARGE = -1, -2, -3, -4
 ERR_OVERLAP, ERR_VARIANT, ERR_CUDA, ERR_ALIGN, ERR_DTYPE, ERR_HOST = -5, -6, -7, -8, -9, -10
-ERR_SCRATCH = -11
+ERR_SCRATCH, ERR_DEVICE = -11, -12
 
 BF16, F16, F32 = 0, 1, 2
 _DTYPE_CODE = {torch.bfloat16: BF16, torch.float16: F16, torch.float32: F32}

@@ -51,7 +51,14 @@ int resolve_ptr(const void *p, const void **dev, bool *host) {
         return GATED_ACT_ERR_HOST;
     }
     switch (a.type) {
-    case cudaMemoryTypeDevice:
+    case cudaMemoryTypeDevice: {
+        // kernels run on the current device: another GPU's memory would be
+        // reached over a peer mapping, if one exists at all
+        int cur = -1;
+        if (cudaGetDevice(&cur) != cudaSuccess || a.device != cur)
+            return GATED_ACT_ERR_DEVICE;
+        return GATED_ACT_OK;
+    }
     case cudaMemoryTypeManaged:
         return GATED_ACT_OK;
     case cudaMemoryTypeHost:
@@ -101,6 +108,7 @@ extern "C" const char *gated_act_status_string(int status) {
     case GATED_ACT_ERR_DTYPE: return "unknown or unsupported element type";
     case GATED_ACT_ERR_HOST: return "memory the CUDA runtime does not know (pageable or unallocated)";
     case GATED_ACT_ERR_SCRATCH: return "needs more scratch than the library's static array holds";
+    case GATED_ACT_ERR_DEVICE: return "device memory of a GPU other than the current one";
     default: return "unknown status";
     }
 }

@@ -30,7 +30,9 @@
  *     place, over the CPU-GPU link, with no separate copy (the bulk-copy
  *     geometries, tma rows and pipe rows, are then not used).  An address
  *     the CUDA runtime does not know -- pageable host memory, or no
- *     allocation at all -- gives GATED_ACT_ERR_HOST with nothing launched.
+ *     allocation at all -- gives GATED_ACT_ERR_HOST, and device memory of
+ *     another GPU than the current one gives GATED_ACT_ERR_DEVICE, both with
+ *     nothing launched.
  *     The activations allocate no memory, never synchronize the host and
  *     launch only on `stream` (0 = the legacy default stream), so every call
  *     is asynchronous and can be captured in a CUDA graph.  The library keeps
@@ -75,7 +77,8 @@ typedef enum gated_act_status {
     GATED_ACT_ERR_ALIGN = -8,      /* a pointer is not aligned to its element size */
     GATED_ACT_ERR_DTYPE = -9,      /* unknown element type                        */
     GATED_ACT_ERR_HOST = -10,      /* memory the CUDA runtime does not know       */
-    GATED_ACT_ERR_SCRATCH = -11    /* more scratch than the static array holds    */
+    GATED_ACT_ERR_SCRATCH = -11,   /* more scratch than the static array holds    */
+    GATED_ACT_ERR_DEVICE = -12     /* device memory of a GPU other than the current one */
 } gated_act_status;
 
 /* Element types of the typed entry point (in and out share one type). */

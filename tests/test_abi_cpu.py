@@ -58,8 +58,19 @@ def test_library_exports_every_declared_symbol(lib):
     assert set(declared_functions()) == set(ga.EXPORTED)
 
 
+def test_status_codes_match_the_header():
+    """Every GATED_ACT_ status the header declares has the same value in the binding."""
+    with open(HEADER) as f:
+        text = f.read()
+    body = text[text.index("typedef enum gated_act_status"):text.index("} gated_act_status;")]
+    codes = dict(re.findall(r"GATED_ACT_(\w+)\s*=\s*(-?\d+)", body))
+    assert len(codes) >= 13, codes
+    for name, value in codes.items():
+        assert getattr(ga, name) == int(value), name
+
+
 def test_status_strings(lib):
-    for code in range(-11, 1):
+    for code in range(-12, 1):
         s = lib.gated_act_status_string(code)
         assert s and s.decode()
     assert lib.gated_act_status_string(-99).decode() == "unknown status"
