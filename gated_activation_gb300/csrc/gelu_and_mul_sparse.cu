@@ -54,7 +54,7 @@ constexpr int kWarpRowsThreads = 128;      // 4 rows per CTA in the warp-rows ge
 constexpr int kMaxCluster = 8;             // portable cluster size
 constexpr int kMaxSliceVec = 4096;         // 16-byte gate vectors one CTA can hold (1024 x 4)
 constexpr int kMinSliceVec = 256;          // slices up to this use 2 vectors per thread
-constexpr int kFewRows = 8;                // up to this many rows of d >= 16384 use clusters
+constexpr int kFewRows = 8;                // the "few rows" unit of the cluster rules
 constexpr int kScalarThreads = 256;
 
 constexpr int kTmaMaxStages = 8;
@@ -1568,15 +1568,20 @@ int make_plan(const void *out, const void *in, int64_t T, int64_t d, int64_t rs,
             while (ceil_div(nvec, C) > kMaxSliceVec && C < kMaxCluster)
                 C *= 2;
             // measured on GB300: 8-CTA clusters for a handful of rows of
-            // d >= 16384, 4-CTA clusters for 9-32 rows of d >= 32768
-            // (T = 16: 3.84 against 4.59 us with one CTA per row), 2-CTA
-            // clusters for 33-64 rows of d >= 32768 (T = 64: 5.36 against
-            // 5.54 us; from 96 rows one CTA per row is 10% faster)
-            if (T <= kFewRows && nvec >= 2048)
+            // d >= 16384, and for up to 32 rows of d = 16384 (T = 16: 2.92
+            // against 3.31 us with one CTA per row; T = 32: 3.28 against
+            // 3.40; T = 40: 3.50 against 3.44); 4-CTA clusters for 9-32 rows
+            // of wider rows (d = 32768, T = 16: 3.84 against 4.59 us with one
+            // CTA per row; d = 20480 and 24576, T = 16: 3.12 and 3.20 against
+            // 3.36 and 3.41 in 8-CTA clusters, 3.81 and 4.04 with one CTA per
+            // row), 2-CTA clusters for 33-64 of them (d = 32768, T = 64: 5.36
+            // against 5.54 us; d = 24576, T = 48: 4.27 against 4.45; from 96
+            // rows one CTA per row is 10% faster)
+            if (nvec >= 2048 && (T <= kFewRows || (T <= 4 * kFewRows && nvec == 2048)))
                 C = kMaxCluster;
-            else if (T <= 4 * kFewRows && nvec >= 4096)
+            else if (T <= 4 * kFewRows && nvec > 2048)
                 C = std::max(C, 4);
-            else if (T <= 8 * kFewRows && nvec >= 4096)
+            else if (T <= 8 * kFewRows && nvec > 2048)
                 C = std::max(C, 2);
         }
         if (C < 1 || C > kMaxCluster || (C & (C - 1)) != 0)

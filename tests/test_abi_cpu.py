@@ -179,7 +179,8 @@ def test_plan_geometry_families(lib):
         assert rc == 0 and p["variant"] == "cta_row" and p["cluster"] == 2, T
         assert p["grid"] == 2 * T and p["threads"] == 512
     assert plan(lib, 65, 32768)[1]["cluster"] == 1
-    assert plan(lib, 16, 16384)[1]["cluster"] == 1
+    assert plan(lib, 16, 16384)[1]["cluster"] == 8      # up to 32 rows of d = 16384
+    assert plan(lib, 40, 16384)[1]["cluster"] == 1
     assert plan(lib, 64, 16384)[1]["cluster"] == 1
     # rows wider than one CTA's registers are split across a cluster
     rc, p = plan(lib, 2048, 65536, variant=ga.VARIANT_CTA_ROW)
@@ -222,6 +223,21 @@ def test_plan_eight_cta_clusters_use_two_vector_slices(lib):
     # 4-CTA clusters keep four vectors per thread
     rc, p = plan(lib, 16, 32768)
     assert rc == 0 and p["cluster"] == 4 and p["vec_per_thread"] == 4
+    # d = 16384: 8-CTA clusters of 128 two-vector threads up to 32 rows, then
+    # one CTA per row
+    for T in (1, 8, 9, 16, 32):
+        rc, p = plan(lib, T, 16384)
+        assert rc == 0 and p["cluster"] == 8 and p["threads"] == 128, (T, p)
+    for T in (33, 64):
+        rc, p = plan(lib, T, 16384)
+        assert rc == 0 and p["cluster"] == 1, (T, p)
+    # between 16384 and 32768: 8-CTA clusters up to 8 rows, 4-CTA clusters to
+    # 32, 2-CTA clusters to 64
+    for d in (20480, 24576):
+        assert plan(lib, 8, d)[1]["cluster"] == 8
+        assert plan(lib, 16, d)[1]["cluster"] == 4
+        assert plan(lib, 33, d)[1]["cluster"] == 2
+        assert plan(lib, 65, d)[1]["cluster"] == 1
 
 
 def test_plan_falls_back_to_scalar(lib):
