@@ -1486,25 +1486,27 @@ int make_plan(const void *out, const void *in, int64_t T, int64_t d, int64_t rs,
     // rotating buffers):
     //  * rows wider than 16384 from about 1.6 rows per SM at d = 32768 on:
     //    pipe rows; with a workspace (dynamic rows) at any T, without one
-    //    while round-robin rows stay below 8 per CTA (d = 32768; beyond that
-    //    a slow SM holds the static split back more than in tma rows);
+    //    while round-robin rows stay below 8 per CTA for d >= 28672 (beyond
+    //    that a slow SM holds the static split back more than in tma rows:
+    //    2048 x 28672, 59.6 against 56.7 us; at d = 24576 the two are within
+    //    2%, at d = 20480 pipe rows stay ahead, 40.5 against 45.9);
     //  * d in [14336, 16384]: pipe rows from 8 rows per SM on, with or
     //    without a workspace (from 6 rows per SM a single launch is faster
     //    too, but among other activation kernels the switch of the SM's
     //    shared-memory split around it costs more than it gains);
     //  * tma rows for the widest rows at many rows per SM;
-    //  * one CTA per row everywhere else, except a handful of rows of
-    //    d >= 16384, where 8-CTA clusters put more SMs on each row.
+    //  * one CTA per row everywhere else, except up to 64 rows wider than
+    //    8192, where clusters put more SMs on each row.
     if (variant == GATED_ACT_VARIANT_AUTO) {
         const int64_t sm = static_cast<int64_t>(sms);
         if (!vec_ok || nvec > int64_t(kMaxSliceVec) * kMaxCluster)
             variant = GATED_ACT_VARIANT_SCALAR;
         else if (pipe_ok && nvec > 2048 && 10 * T * nvec >= 16 * sm * 4096 &&
-                 (has_ws || nvec < 4096 || T < 8 * sm))
+                 (has_ws || nvec < 3584 || T < 8 * sm))
             variant = GATED_ACT_VARIANT_PIPE_ROWS;
         else if (pipe_ok && nvec >= 1792 && nvec <= 2048 && T >= 8 * sm)
             variant = GATED_ACT_VARIANT_PIPE_ROWS;
-        else if (tma_ok && ((nvec >= 4096 && T >= 3 * sm) || (nvec >= 2048 && T >= 12 * sm)))
+        else if (tma_ok && ((nvec >= 3584 && T >= 3 * sm) || (nvec >= 2048 && T >= 12 * sm)))
             variant = GATED_ACT_VARIANT_TMA_ROWS;
         else if (nvec <= 64 && !cta_only)
             variant = GATED_ACT_VARIANT_WARP_ROWS;
@@ -1567,17 +1569,25 @@ int make_plan(const void *out, const void *in, int64_t T, int64_t d, int64_t rs,
             C = 1;
             while (ceil_div(nvec, C) > kMaxSliceVec && C < kMaxCluster)
                 C *= 2;
-            // measured on GB300: 8-CTA clusters for a handful of rows of
-            // d >= 16384, and for up to 32 rows of d = 16384 (T = 16: 2.92
-            // against 3.31 us with one CTA per row; T = 32: 3.28 against
-            // 3.40; T = 40: 3.50 against 3.44); 4-CTA clusters for 9-32 rows
-            // of wider rows (d = 32768, T = 16: 3.84 against 4.59 us with one
+            // measured on GB300 (every cluster size at T = 1...96 for d =
+            // 8192 ... 32768): 8-CTA clusters for up to 8 rows wider than
+            // 8192 (d = 9216, T = 1: 2.29 against 2.72 us with one CTA per
+            // row, whose CTA then has 1024 threads; at d = 8192 one CTA of
+            // 512 threads is 2-5% faster), up to 16 rows of d <= 16384
+            // (d = 11008, T = 16: 2.89 against 2.99) and up to 32 rows of
+            // d = 14336 ... 16384 (d = 16384, T = 32: 3.28 against 3.40;
+            // T = 40: 3.50 against 3.44); 4-CTA clusters for 9-32 rows of
+            // wider rows (d = 32768, T = 16: 3.84 against 4.59 us with one
             // CTA per row; d = 20480 and 24576, T = 16: 3.12 and 3.20 against
             // 3.36 and 3.41 in 8-CTA clusters, 3.81 and 4.04 with one CTA per
             // row), 2-CTA clusters for 33-64 of them (d = 32768, T = 64: 5.36
             // against 5.54 us; d = 24576, T = 48: 4.27 against 4.45; from 96
             // rows one CTA per row is 10% faster)
-            if (nvec >= 2048 && (T <= kFewRows || (T <= 4 * kFewRows && nvec == 2048)))
+            const bool eight =
+                nvec > 1024 &&
+                (T <= kFewRows ||
+                 (nvec <= 2048 && (T <= 2 * kFewRows || (nvec >= 1792 && T <= 4 * kFewRows))));
+            if (eight)
                 C = kMaxCluster;
             else if (T <= 4 * kFewRows && nvec > 2048)
                 C = std::max(C, 4);

@@ -136,10 +136,14 @@ def test_widened_rows_reject_bad_arguments(lib):
 
 
 def plan(lib, T, d, rs=None, variant=0, cluster=0, sms=GB300_SMS, out=0x10000, inp=0x100000,
-         dtype=0):
+         dtype=0, ws=0):
     p = ga.Plan()
-    rc = lib.gelu_and_mul_sparse_plan(out, inp, T, d, rs or 2 * d, dtype, variant, cluster, sms,
-                                      ctypes.byref(p))
+    if ws:
+        rc = lib.gelu_and_mul_sparse_plan_ex(out, inp, T, d, rs or 2 * d, dtype, variant, cluster,
+                                             sms, 1, ctypes.byref(p))
+    else:
+        rc = lib.gelu_and_mul_sparse_plan(out, inp, T, d, rs or 2 * d, dtype, variant, cluster,
+                                          sms, ctypes.byref(p))
     return rc, p.as_dict()
 
 
@@ -231,6 +235,17 @@ def test_plan_eight_cta_clusters_use_two_vector_slices(lib):
     for T in (33, 64):
         rc, p = plan(lib, T, 16384)
         assert rc == 0 and p["cluster"] == 1, (T, p)
+    # above 8192 up to 16384: 8-CTA clusters up to 8 rows, 16 rows, and 32
+    # rows from 14336
+    for T, d, c in ((8, 8192, 1), (1, 9216, 8), (8, 9216, 8), (16, 11008, 8), (17, 11008, 1),
+                    (24, 12288, 1), (24, 14336, 8), (32, 14336, 8), (33, 14336, 1)):
+        rc, p = plan(lib, T, d)
+        assert rc == 0 and p["variant"] == "cta_row" and p["cluster"] == c, (T, d, p)
+    # without a workspace, many rows of d >= 28672 take tma rows
+    assert plan(lib, 2048, 28672)[1]["variant"] == "tma_rows"
+    assert plan(lib, 1219, 28672)[1]["variant"] == "tma_rows"
+    assert plan(lib, 1215, 28672)[1]["variant"] == "pipe_rows"
+    assert plan(lib, 2048, 28672, ws=1)[1]["variant"] == "pipe_rows"
     # between 16384 and 32768: 8-CTA clusters up to 8 rows, 4-CTA clusters to
     # 32, 2-CTA clusters to 64
     for d in (20480, 24576):

@@ -59,12 +59,14 @@ def test_decode_forced_clusters(ga, oracle, cluster):
     check_gelu(out, inp.x, inp.d, res, f"decode16 c{cluster}")
 
 
-# rows of d = 16384 that the plan spreads over 8-CTA clusters (up to 32), the
-# first count past that rule, and rows between 16384 and 32768 wide in 4- and
+# few rows wider than 8192 that the plan spreads over clusters: 8-CTA
+# clusters (up to 8 rows, 16 up to d = 16384, 32 from d = 14336), the first
+# counts past those rules, and rows between 16384 and 32768 wide in 4- and
 # 2-CTA clusters (rows = T random rows + 3 constant rows)
 @pytest.mark.parametrize("rows,d,cluster", [(9, 16384, 8), (16, 16384, 8), (24, 16384, 8),
                                             (32, 16384, 8), (33, 16384, 1), (16, 20480, 4),
-                                            (32, 24576, 4), (48, 24576, 2)])
+                                            (32, 24576, 4), (48, 24576, 2), (4, 9216, 8),
+                                            (16, 11008, 8), (17, 11008, 1), (24, 14336, 8)])
 def test_wide_few_rows_in_clusters(ga, oracle, rows, d, cluster):
     inp = W.sweep(rows - 3, d, z=W.Z95, const_rows=True)
     assert inp.x.shape[0] == rows
@@ -72,6 +74,15 @@ def test_wide_few_rows_in_clusters(ga, oracle, rows, d, cluster):
     assert plan["variant"] == "cta_row" and plan["cluster"] == cluster, plan
     res = oracle_of(oracle, inp.x, inp.d, inp.z)
     check_gelu(run(ga, inp.x, inp.d, inp.z), inp.x, inp.d, res, f"{inp.name} plan c{cluster}")
+
+
+# many rows of d = 28672 without a workspace: tma rows (round-robin rows)
+def test_wide_rows_without_workspace_take_tma_rows(ga, oracle):
+    inp = W.sweep(1216, 28672, z=W.Z95, const_rows=True)
+    plan = ga.gelu_and_mul_sparse_plan(inp.x.cuda(), d=inp.d)
+    assert plan["variant"] == "tma_rows", plan
+    res = oracle_of(oracle, inp.x, inp.d, inp.z)
+    check_gelu(run(ga, inp.x, inp.d, inp.z), inp.x, inp.d, res, f"{inp.name} tma rows")
 
 
 def test_prefill_full(ga, oracle):
