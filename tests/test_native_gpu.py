@@ -54,6 +54,22 @@ def test_native_constant_rows_and_ragged(ga, oracle, dt):
         check_native(run(ga, inp.x, d, inp.z), inp.x, d, ref, mask, cut, f"{dt} d{d}", z=inp.z)
 
 
+# native rows spread over clusters (rows = T random rows + 3 constant rows):
+# 8-CTA clusters for a few rows above d = 8192, 4- and 2-CTA clusters for
+# more rows above 16384
+@pytest.mark.parametrize("rows,d,cluster", [(4, 16384, 8), (16, 14336, 8), (4, 9216, 8),
+                                            (19, 24576, 4), (48, 32768, 2)])
+@pytest.mark.parametrize("dt", DTYPES)
+def test_native_cluster_rows(ga, oracle, dt, rows, d, cluster):
+    inp = W.sweep(rows - 3, d, dtype=dt)
+    plan = ga.gelu_and_mul_sparse_native_plan(inp.x.cuda(), d=d)
+    assert plan["variant"] == "cta_row" and plan["cluster"] == cluster, plan
+    ref, mask, cut = oracle_native(oracle, inp.x, d, inp.z)
+    out = run(ga, inp.x, d, inp.z)
+    check_native(out, inp.x, d, ref, mask, cut, f"{dt} {inp.name} c{cluster}", z=inp.z)
+    assert torch.count_nonzero(out[-3:].float()).item() == 0
+
+
 @pytest.mark.parametrize("dt", DTYPES)
 def test_native_reproduces_torch_cuda_composition(ga, dt):
     # PyTorch's own composition of separate element-type ops on the GPU: the
