@@ -656,7 +656,12 @@ gelu_tma_rows(uint16_t *__restrict__ out, const uint16_t *__restrict__ in, int64
 // and an "empty" one (one arrive per consumer warp once the slot has been
 // read), so copy issue and ticket round trips run beside the consumers, who
 // synchronise among themselves with a named barrier only.  Chunk c (gate of
-// the CTA's row c/2 for even c, up for odd c) uses slot c mod S.
+// the CTA's job c/2 for even c, up for odd c) uses slot c mod S.
+// A job is a row, or with dynamic rows one half of one of the last `split`
+// rows: its CTA reads the whole gate half-row (the statistics need it; both
+// halves compute the same bits) but only its half of the up half-row, and
+// writes that half of the output row.  Splitting the last wave of rows
+// halves the epilogue that ends the launch on the SMs that finish last.
 // Failure handling: every wait is bounded.  Consumers that give up vote to
 // stop together and leave their slots unreleased; the producer notices
 // (cons_done), stops issuing, and waits (bounded) for its own copies in
@@ -686,11 +691,20 @@ __device__ __forceinline__ float cons_sum(float v, float *red, int lane, int war
 }
 
 constexpr int kPipeMaxStages = 16;
+// Half jobs for the last rows of a pipe-rows launch with dynamic rows: one
+// row per CTA, from 3 rows per CTA at d >= 32768.  Measured on GB300 at
+// d = 32768: 1024 rows 32.66 -> 32.34 us, 2048 rows 60.67 -> 59.77, 4096
+// rows 115.86 -> 114.65; splitting half or a quarter as many rows gained
+// nothing; at 256 and 384 rows, and at d = 16384 and 20480, splitting lost
+// 2-6% (the second read of the gate half-row costs more than it saves).
+constexpr int64_t kPipeSplitDiv = 1;           // split rows: grid / this
+constexpr int64_t kPipeSplitMinVec = 4096;
+constexpr int64_t kPipeSplitMinRowsPerCta = 3;
 
 template <int NCW, int V>
 __global__ void __launch_bounds__((NCW + 1) * 32, (NCW >= 16 ? 1 : NCW >= 8 ? 2 : 4))
 gelu_pipe_rows(uint16_t *__restrict__ out, const uint16_t *__restrict__ in, int64_t T, int d,
-               int64_t rs, float z, int S, unsigned long long *__restrict__ sched,
+               int64_t rs, float z, int S, unsigned long long *__restrict__ sched, int64_t split,
                int64_t withhold, unsigned long long wait_ns) {
     constexpr int NC = NCW * 32;
     extern __shared__ __align__(128) uint8_t smem[];
@@ -738,7 +752,13 @@ gelu_pipe_rows(uint16_t *__restrict__ out, const uint16_t *__restrict__ in, int6
                     return false;
             }
         };
+        // jobs: rows 0 .. T - split - 1 whole, then each of the last `split`
+        // rows as two half jobs (both CTAs read the whole gate half-row for
+        // the statistics; each reads, computes and writes half of the up
+        // and output columns)
+        const int64_t J = T + split, whole = T - split;
         int64_t c = 0, row = 0, claimed = 0;
+        int half = -1;   // -1: the whole row, else which half of it
         uint32_t slot = 0, round = 0;
         bool ended = false, bad = false;
         for (;; ++c) {
@@ -746,28 +766,32 @@ gelu_pipe_rows(uint16_t *__restrict__ out, const uint16_t *__restrict__ in, int6
                 bad = true;
                 break;
             }
-            if ((c & 1) == 0) {   // a gate chunk: the CTA's next row
-                row = claimed == 0 ? static_cast<int64_t>(blockIdx.x)
-                      : sched      ? G + static_cast<int64_t>(atomicAdd(sched, 1ull))
-                                   : static_cast<int64_t>(blockIdx.x) + claimed * G;
+            if ((c & 1) == 0) {   // a gate chunk: the CTA's next job
+                const int64_t j = claimed == 0 ? static_cast<int64_t>(blockIdx.x)
+                                  : sched      ? G + static_cast<int64_t>(atomicAdd(sched, 1ull))
+                                               : static_cast<int64_t>(blockIdx.x) + claimed * G;
                 ++claimed;
-                if (row >= T) {
+                if (j >= J) {
                     slot_row[slot] = -1;
                     mbar_arrive(full + 8u * slot);
-                    if (sched && row == G + T - 1)   // ticket T - 1: reset the counter
+                    if (sched && j == G + J - 1)   // ticket J - 1: reset the counter
                         asm volatile("red.relaxed.gpu.global.and.b64 [%0], %1;" ::"l"(sched),
                                      "l"(0ull)
                                      : "memory");
                     ended = true;
                     break;
                 }
-                slot_row[slot] = row;
+                row = j < whole ? j : whole + ((j - whole) >> 1);
+                half = j < whole ? -1 : static_cast<int>((j - whole) & 1);
+                slot_row[slot] = 4 * row + (half + 1);
             }
             if (c != withhold) {
+                // an up chunk of a half job: d bytes (half the up half-row)
+                const uint32_t bytes = ((c & 1) && half >= 0) ? chunk / 2 : chunk;
+                const int64_t col = (c & 1) ? d + (half > 0 ? d / 2 : 0) : 0;
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                mbar_expect_tx(full + 8u * slot, chunk);
-                bulk_load(base + slot * chunk, in + row * rs + ((c & 1) ? d : 0), chunk,
-                          full + 8u * slot);
+                mbar_expect_tx(full + 8u * slot, bytes);
+                bulk_load(base + slot * chunk, in + row * rs + col, bytes, full + 8u * slot);
             }
             if (++slot == nslots) {
                 slot = 0;
@@ -787,9 +811,9 @@ gelu_pipe_rows(uint16_t *__restrict__ out, const uint16_t *__restrict__ in, int6
         // one, so the launch hands out exactly T and one CTA resets the counter
         if (sched && !ended) {
             int64_t r = -1;
-            while (r < T)
+            while (r < J)
                 r = G + static_cast<int64_t>(atomicAdd(sched, 1ull));
-            if (r == G + T - 1)
+            if (r == G + J - 1)
                 asm volatile("red.relaxed.gpu.global.and.b64 [%0], %1;" ::"l"(sched), "l"(0ull)
                              : "memory");
         }
@@ -812,7 +836,7 @@ gelu_pipe_rows(uint16_t *__restrict__ out, const uint16_t *__restrict__ in, int6
         next(&sg, &pg);
         next(&su, &pu);
         bad |= !mbar_wait(full + 8u * sg, pg, wait_ns);
-        const int64_t row = slot_row[sg];
+        const int64_t tag = slot_row[sg];   // 4 row + (half + 1), or -1 at the end
         const uint4 *gs = reinterpret_cast<const uint4 *>(smem + static_cast<size_t>(sg) * chunk);
         uint4 g[V];
 #pragma unroll
@@ -829,8 +853,10 @@ gelu_pipe_rows(uint16_t *__restrict__ out, const uint16_t *__restrict__ in, int6
             red[0][warp] = s;
         // both exits are uniform over the consumers: the vote, and the end
         // mark every consumer read after the same completed phase
-        if (cons_sync_or<NCW>(bad) || row < 0)
+        if (cons_sync_or<NCW>(bad) || tag < 0)
             break;
+        const int64_t row = tag >> 2;
+        const int half = static_cast<int>(tag & 3) - 1;
         if (lane == 0)
             mbar_arrive(empty + 8u * sg);   // the gate half-row is in registers
         s = warp_sum(lane < NCW ? red[0][lane] : 0.f);
@@ -850,11 +876,14 @@ gelu_pipe_rows(uint16_t *__restrict__ out, const uint16_t *__restrict__ in, int6
         if (!bad) {
             const uint4 *us = reinterpret_cast<const uint4 *>(smem + static_cast<size_t>(su) * chunk);
             uint16_t *op = out + row * static_cast<int64_t>(d);
+            // the columns of this job: all, or one half (nvec is even then)
+            const int vlo = half > 0 ? nvec >> 1 : 0;
+            const int vhi = half == 0 ? nvec >> 1 : nvec;
 #pragma unroll
             for (int i = 0; i < V; ++i) {
                 const int v = tid + NC * i;
-                if (v < nvec)
-                    st_vec(op + 8 * v, epi_vec<FmtBf16>(g[i], us[v], cutoff));
+                if (v >= vlo && v < vhi)
+                    st_vec(op + 8 * v, epi_vec<FmtBf16>(g[i], us[v - vlo], cutoff));
             }
         }
         // a warp that missed the up half-row keeps its slot (its copy may
@@ -1193,6 +1222,8 @@ using CtaFn = void (*)(void *, const void *, int64_t, int, int64_t, float, int, 
 using ScalarFn = void (*)(void *, const void *, int64_t, int64_t, int64_t, float);
 using TmaFn = void (*)(uint16_t *, const uint16_t *, int64_t, int, int64_t, float, int,
                       unsigned long long *, int64_t, unsigned long long);
+using PipeFn = void (*)(uint16_t *, const uint16_t *, int64_t, int, int64_t, float, int,
+                        unsigned long long *, int64_t, int64_t, unsigned long long);
 
 WarpFn warp_fn(int v) {
     switch (v) {
@@ -1277,7 +1308,7 @@ TmaFn tma_fn(int nt) {
 }
 
 // Pipe rows: NCW consumer warps x V gate vectors per consumer thread.
-TmaFn pipe_fn(int ncw, int v) {
+PipeFn pipe_fn(int ncw, int v) {
     switch (ncw * 16 + v) {
     case 16 * 16 + 8: return gelu_pipe_rows<16, 8>;
     case 16 * 16 + 4: return gelu_pipe_rows<16, 4>;
@@ -1672,7 +1703,8 @@ unsigned long long current_context_id() {
 // context (after cudaDeviceReset, or one the caller made current) sets them
 // again, and where the context id is unavailable they are set on every call.
 // key: a bit index in [0, 32) that names the kernel.
-int ensure_smem_attr(TmaFn fn, int key) {
+template <class Fn>
+int ensure_smem_attr(Fn fn, int key) {
     constexpr int kMaxDevices = 64;
     struct Entry {
         unsigned long long ctx;
@@ -1710,6 +1742,14 @@ int ensure_smem_attr(TmaFn fn, int key) {
     return GATED_ACT_OK;
 }
 
+// Pipe rows with dynamic rows: how many of the last rows run as two half
+// jobs (rows of an even number of 16-byte vectors only).
+int64_t pipe_split_rows(int64_t T, int64_t nvec, int64_t grid) {
+    if (nvec % 2 != 0 || nvec < kPipeSplitMinVec || T < kPipeSplitMinRowsPerCta * grid)
+        return 0;
+    return std::min<int64_t>(T, grid / kPipeSplitDiv);
+}
+
 // workspace: zeroed counters for dynamic rows (bulk-copy geometry with
 // dynamic_rows set), else ignored.
 int launch(const Plan &p, void *out, const void *in, int64_t T, int64_t d, int64_t rs,
@@ -1738,7 +1778,7 @@ int launch(const Plan &p, void *out, const void *in, int64_t T, int64_t d, int64
     }
     case GATED_ACT_VARIANT_PIPE_ROWS: {
         const int ncw = q.threads / 32 - 1;
-        TmaFn fn = pipe_fn(ncw, q.vec_per_thread);
+        PipeFn fn = pipe_fn(ncw, q.vec_per_thread);
         if (!fn)
             return GATED_ACT_ERR_VARIANT;
         const int rc = ensure_smem_attr(fn, 16 + ncw / 4 + q.vec_per_thread);
@@ -1746,8 +1786,10 @@ int launch(const Plan &p, void *out, const void *in, int64_t T, int64_t d, int64
             return rc;
         unsigned long long *sched =
             q.dynamic_rows ? static_cast<unsigned long long *>(workspace) : nullptr;
+        const int64_t split = sched ? pipe_split_rows(T, d / 8, q.grid) : 0;
         e = launch_kernel(fn, grid, block, static_cast<size_t>(q.smem_bytes), stream, 1, o, x, T,
-                          di, rs, zf, static_cast<int>(q.stages), sched, withhold, wait_ns);
+                          di, rs, zf, static_cast<int>(q.stages), sched, split, withhold,
+                          wait_ns);
         break;
     }
     case GATED_ACT_VARIANT_WARP_ROWS:

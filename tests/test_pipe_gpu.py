@@ -1,7 +1,8 @@
 """The producer/consumer geometry (gelu_pipe_rows): parity with the oracle at
 every CTAs-per-SM setting it supports, round-robin and dynamic rows (bitwise
-equal to each other), ragged widths, guard bands, the workspace left zeroed,
-and its give-up path without a fault."""
+equal to each other, the latter with its last rows split in half jobs at
+d = 32768), ragged widths, guard bands, the workspace left zeroed, and its
+give-up path without a fault."""
 import numpy as np
 import pytest
 import torch
@@ -29,7 +30,10 @@ CASES = [(1, 2048, 0), (7, 4096, 4), (300, 4096, 4), (2000, 1000, 0), (5000, 204
          (700, 8192, 2), (2500, 8192, 4), (1300, 8192, 1), (333, 12296, 0), (640, 16384, 2),
          (2048, 16384, 1), (160, 32768, 1), (3, 32768, 0), (1000, 32768, 1),
          # widths between the powers of two, and an odd vector count
-         (300, 20480, 0), (600, 24576, 0), (200, 32760, 0), (257, 16392, 0)]
+         (300, 20480, 0), (600, 24576, 0), (200, 32760, 0), (257, 16392, 0),
+         # dynamic rows with the last rows split in half jobs: just above the
+         # threshold (3 rows per CTA), and more rows per CTA
+         (460, 32768, 0), (1500, 32768, 0)]
 
 
 @pytest.mark.parametrize("T,d,cps", CASES)
@@ -51,7 +55,8 @@ def test_pipe_rows_match_oracle_static_and_dynamic(ga, oracle, T, d, cps):
     assert guards_intact(buf_s) and guards_intact(buf_d)
     assert bool((ws == 0).all().item()), "workspace not left zeroed"
     assert ga.device_status() == 0
-    assert torch.equal(_bits(dyn), _bits(stat)), "one CTA computes each row either way"
+    # whole rows or half jobs: the same statistics and arithmetic, so the same bits
+    assert torch.equal(_bits(dyn), _bits(stat)), "dynamic rows differ from round-robin rows"
     res = oracle.gelu_and_mul_sparse(W.to_bits(inp.x), d=d, z=inp.z)
     check_gelu(stat.cpu(), inp.x, d, res, f"pipe T{T} d{d} cps{cps}")
 
