@@ -329,12 +329,15 @@ int gelu_and_mul_sparse_native_plan(const void *out, const void *in, int64_t T,
  * round-robin rows, each CTA ends when its own share is done, and the SMs
  * that stream more slowly set the end of the launch.  With a workspace the
  * CTAs instead take rows from an atomic counter in it, so every SM stays
- * busy to the end.  Within one geometry the results are identical: every row
- * is still computed by one CTA in the same order.  The automatic choice can
- * differ with a workspace: for rows wider than 16384 it prefers pipe rows,
- * which gain most from dynamic rows, where the plain call keeps tma rows
- * (d = 32768 from 8 rows per SM on).  Then the two calls agree within the
- * accuracy bound rather than bitwise; gelu_and_mul_sparse_plan_ex tells.
+ * busy to the end; at d >= 32768 pipe rows also run the last wave of rows
+ * as two half jobs each (both compute the row's statistics in full, each
+ * writes half of its output).  Within one geometry the results are
+ * identical: every row's statistics and outputs are computed in the same
+ * order either way.  The automatic choice can differ with a workspace: for
+ * rows wider than 16384 it prefers pipe rows, which gain most from dynamic
+ * rows, where the plain call keeps tma rows (d >= 28672 from 8 rows per SM
+ * on).  Then the two calls agree within the accuracy bound rather than
+ * bitwise; gelu_and_mul_sparse_plan_ex tells.
  * ------------------------------------------------------------------------ */
 
 /* Bytes of workspace gelu_and_mul_sparse_ws needs (a constant, 16). */
