@@ -18,7 +18,10 @@
 //                    CTA takes the next ticket of an atomic counter;
 //   * pipe rows   -- as tma rows, warp-specialised: one lane of a producer
 //                    warp issues every copy and takes every ticket, the other
-//                    warps finish rows; full/empty mbarriers per slot;
+//                    warps finish rows; full/empty mbarriers per slot.  With
+//                    tickets, the last wave of the widest rows runs as half
+//                    jobs that both copy the row's gate half (the second
+//                    copy is normally still in L2) and split its columns;
 //   * warp rows   -- one warp per row, shuffles only (d <= 2048);
 //   * CTA row     -- one CTA per row, or a cluster of C CTAs per row, each CTA
 //                    holding a column slice in registers; in a cluster every
