@@ -91,19 +91,36 @@ __device__ __forceinline__ float tanh_approx(float x) {
     return y;
 }
 
+// gelu_tanh(s) = 0.5 s (1 + tanh(y)) = s / (1 + e^{-2y}) for fp32 outputs,
+// y >= 0: e^{-2y} in (0, 1] from the flushing hardware exponential (PTX ISA
+// ex2.approx.ftz.f32, relative error about 2^-22; below 2^-126, past y = 43.7,
+// it flushes to 0 and the result is s, the exact limit), 1 + e^{-2y} in (1, 2]
+// inverted by the flushing hardware reciprocal (rcp.approx.ftz.f32, within
+// one ulp there).  Relative error about 2^-21, with no cancellation since
+// nothing is subtracted.
+__device__ __forceinline__ float gelu_exp_form(float s, float y) {
+    float e, r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(y * (-2.0f * 1.4426950408889634f)));
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + e));
+    return s * r;
+}
+
 // ------------------------------------------------------------ element formats
 // A 16-byte vector holds kPairs pairs of elements: pair(v, i) reads pair i as
-// fp32, put_pair writes pair i rounded to the format (nearest even).  tanh is
-// the hardware approximation for the 16-bit formats (its 2^-12 relative error
-// in 1 + tanh is below their rounding) and the accurate libm-style tanhf for
-// fp32 outputs.
+// fp32, put_pair writes pair i rounded to the format (nearest even).
+// gelu_a(s, y, h) is gelu_tanh(s) for a pair (y = sqrt(2/pi)(s + 0.044715 s^3),
+// h = s/2): h + h tanh(y) on the hardware tanh for the 16-bit formats (its
+// 2^-12 relative error in 1 + tanh is below their rounding), the exponential
+// form above for fp32 outputs.
 struct FmtBf16 {
     static constexpr int kElem = 2, kPairs = 4, kLut = 0;   // kLut: native table index
     __device__ static float2 pair(const uint4 &v, int i) { return unpack2((&v.x)[i]); }
     __device__ static void put_pair(uint4 &v, int i, float2 f) {
         (&v.x)[i] = pack_bf16x2(f.x, f.y);
     }
-    __device__ static float tanh(float x) { return tanh_approx(x); }
+    __device__ static float2 gelu_a(float2 s, float2 y, float2 h) {
+        return fma2(h, make_float2(tanh_approx(y.x), tanh_approx(y.y)), h);
+    }
     __device__ static float load1(const uint8_t *p) {
         return __uint_as_float(static_cast<uint32_t>(ld_stream_u16(reinterpret_cast<const uint16_t *>(p))) << 16);
     }
@@ -122,7 +139,9 @@ struct FmtF16 {
         const __half2 h = __floats2half2_rn(f.x, f.y);
         (&v.x)[i] = *reinterpret_cast<const uint32_t *>(&h);
     }
-    __device__ static float tanh(float x) { return tanh_approx(x); }
+    __device__ static float2 gelu_a(float2 s, float2 y, float2 h) {
+        return fma2(h, make_float2(tanh_approx(y.x), tanh_approx(y.y)), h);
+    }
     __device__ static float load1(const uint8_t *p) {
         return __half2float(__ushort_as_half(ld_stream_u16(reinterpret_cast<const uint16_t *>(p))));
     }
@@ -146,7 +165,9 @@ struct FmtF32 {
             v.w = __float_as_uint(f.y);
         }
     }
-    __device__ static float tanh(float x) { return tanhf(x); }
+    __device__ static float2 gelu_a(float2 s, float2 y, float2) {
+        return make_float2(gelu_exp_form(s.x, y.x), gelu_exp_form(s.y, y.y));
+    }
     __device__ static float load1(const uint8_t *p) {
         return __uint_as_float(ld_stream_u32(reinterpret_cast<const uint32_t *>(p)));
     }
@@ -166,7 +187,7 @@ __device__ __forceinline__ uint4 epi_vec(const uint4 &g, const uint4 &u, float c
         const float2 y = mul2(s, fma2(mul2(s, s), make_float2(kCubicCoef, kCubicCoef),
                                       make_float2(kSqrt2OverPi, kSqrt2OverPi)));
         const float2 h = mul2(s, make_float2(0.5f, 0.5f));
-        const float2 a = fma2(h, make_float2(F::tanh(y.x), F::tanh(y.y)), h);
+        const float2 a = F::gelu_a(s, y, h);
         F::put_pair(o, i, mul2(a, F::pair(u, i)));
     }
     return o;
@@ -1174,11 +1195,11 @@ gelu_cta_rows(void *__restrict__ out_, const void *__restrict__ in_, int64_t T, 
 // ------------------------------------------------------------ scalar rows
 // Any layout: one CTA per row, one element per access; each pass re-reads
 // the gate (from L1/L2 after the first pass).
-__device__ __forceinline__ float sparse_gelu_mul(float g, float u, float cutoff, bool exact_tanh) {
+__device__ __forceinline__ float sparse_gelu_mul(float g, float u, float cutoff, bool exp_form) {
     const float s = relu_nan(g - cutoff);
     const float y = s * fmaf(kCubicCoef, s * s, kSqrt2OverPi);
     const float h = 0.5f * s;
-    return fmaf(h, exact_tanh ? tanhf(y) : tanh_approx(y), h) * u;
+    return (exp_form ? gelu_exp_form(s, y) : fmaf(h, tanh_approx(y), h)) * u;
 }
 
 template <class F, bool NATIVE>

@@ -277,8 +277,9 @@ int gelu_and_mul_sparse_ex(void *out, const void *in, int64_t T, int64_t d,
  *   variant, cluster as in gelu_and_mul_sparse_ex.  fp16 and fp32 run the
  *            CTA-row (or scalar) geometry only: WARP_ROWS and TMA_ROWS
  *            return GATED_ACT_ERR_VARIANT for them.
- * Math is fp32 throughout; the fp32 output uses an accurate tanh, the 16-bit
- * outputs the hardware approximation.  Accuracy against an fp64 evaluation:
+ * Math is fp32 throughout; the fp32 output evaluates tanh-GELU as
+ * s / (1 + e^{-2y}) on the hardware exponential and reciprocal (relative
+ * error about 2^-21), the 16-bit outputs use the hardware tanh.  Accuracy against an fp64 evaluation:
  * bf16 1e-2 |ref| + 2e-3; fp16 1e-3 |ref| + 1e-5; fp32 1e-5 |ref| + 1e-5;
  * the zero pattern as for gelu_and_mul_sparse.
  */
