@@ -781,7 +781,10 @@ def link_ceiling(h2d: int, d2h: int, dev) -> dict:
         up()
         down()
 
-    t_both, t_up, t_down = timed(both), timed(up), timed(down)
+    # best of three timings each: the ceiling is what the link can carry, and a
+    # stray stall in one timing (seen once as half the one-direction rate for
+    # both directions at once) must not lower it
+    t_both, t_up, t_down = (min(timed(fn) for _ in range(3)) for fn in (both, up, down))
     return {"value": round((n_in + n_out) / t_both / 1e9, 1), "unit": "GB/s",
             "h2d_alone": round(n_in / t_up / 1e9, 1), "d2h_alone": round(n_out / t_down / 1e9, 1),
             "mix_h2d_to_d2h": round(h2d / max(d2h, 1), 3),
