@@ -28,8 +28,9 @@ BF16, F16, F32 = 0, 1, 2
 _DTYPE_CODE = {torch.bfloat16: BF16, torch.float16: F16, torch.float32: F32}
 
 VARIANT_AUTO, VARIANT_WARP_ROWS, VARIANT_CTA_ROW, VARIANT_SCALAR, VARIANT_TMA_ROWS = 0, 1, 2, 3, 4
-VARIANT_PIPE_ROWS = 5
-VARIANT_NAMES = {0: "auto", 1: "warp_rows", 2: "cta_row", 3: "scalar", 4: "tma_rows", 5: "pipe_rows"}
+VARIANT_PIPE_ROWS, VARIANT_SPLIT_ROWS = 5, 6
+VARIANT_NAMES = {0: "auto", 1: "warp_rows", 2: "cta_row", 3: "scalar", 4: "tma_rows", 5: "pipe_rows",
+                 6: "split_rows"}
 
 EXPORTED = (
     "gelu_and_mul_sparse", "gelu_and_mul_sparse_typed", "gelu_and_mul_sparse_native",

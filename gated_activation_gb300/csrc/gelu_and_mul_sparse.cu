@@ -1192,6 +1192,79 @@ gelu_cta_rows(void *__restrict__ out_, const void *__restrict__ in_, int64_t T, 
     }
 }
 
+// ------------------------------------------------------------ split rows
+// A few wide rows, C independent CTAs per row (no cluster).  Each CTA reads
+// the row's whole gate half and computes the row's statistics itself, in the
+// same order as the other CTAs of the row, so all of them hold the same bits;
+// then it does the epilogue of its slice [k sv, (k+1) sv) of the columns.
+// The C reads of a gate half-row arrive together and L2 serves all but the
+// first, so nothing is exchanged between CTAs: measured on GB300 this beats
+// the cluster exchange (0.6-1.2 us per row) from 9 rows on while all CTAs fit
+// one wave.  Thread t holds gate vectors t + NT i (i < V, the whole row) for
+// the statistics and, for the epilogue, the slice's vectors v0 + t + NT j
+// (j < U) of gate and up.
+template <int NT, int V, int U, class F>
+__global__ void __launch_bounds__(NT, 1)
+gelu_split_rows(void *__restrict__ out_, const void *__restrict__ in_, int64_t T, int d,
+                int64_t rs, float z, int C, int sv) {
+    constexpr int NW = NT / 32;
+    constexpr int kEpv = 16 / F::kElem;
+    __shared__ float red[2][NW];
+    const uint8_t *in = static_cast<const uint8_t *>(in_);
+    uint8_t *out = static_cast<uint8_t *>(out_);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nvec = d / kEpv;
+    const int64_t rs_bytes = rs * F::kElem, d_bytes = static_cast<int64_t>(d) * F::kElem;
+    pdl_wait();
+    pdl_trigger();
+    for (int64_t b = blockIdx.x; b < T * C; b += gridDim.x) {
+        const int64_t row = b / C;
+        const int v0 = static_cast<int>(b - row * C) * sv;
+        const int v1 = min(nvec, v0 + sv);
+        const uint8_t *gp = in + row * rs_bytes;
+        const uint8_t *up = gp + d_bytes;
+        uint4 g[V], gs[U], u[U];
+#pragma unroll
+        for (int i = 0; i < V; ++i) {
+            const int v = tid + NT * i;
+            g[i] = v < nvec ? ld_stream(gp + 16 * v) : make_uint4(0u, 0u, 0u, 0u);   // +0
+        }
+#pragma unroll
+        for (int j = 0; j < U; ++j) {
+            const int v = v0 + tid + NT * j;
+            if (v < v1) {
+                gs[j] = ld_stream(gp + 16 * v);
+                u[j] = ld_stream(up + 16 * v);
+            } else {
+                gs[j] = u[j] = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+        float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < V; ++i)
+            acc = sum_vec<F>(acc, g[i]);
+        const float mean =
+            __fdiv_rn(block_sum<NW>(acc.x + acc.y, red[0], lane, warp), static_cast<float>(d));
+        const float2 m2 = make_float2(mean, mean);
+        acc = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < V; ++i)
+            if (tid + NT * i < nvec)
+                acc = ssd_vec<F>(acc, g[i], m2);
+        const float var =
+            __fdiv_rn(block_sum<NW>(acc.x + acc.y, red[1], lane, warp), static_cast<float>(d));
+        const float cutoff = fmaf(__fsqrt_rn(var), z, mean);
+        uint8_t *op = out + row * d_bytes;
+#pragma unroll
+        for (int j = 0; j < U; ++j) {
+            const int v = v0 + tid + NT * j;
+            if (v < v1)
+                st_vec(op + 16 * v, epi_vec<F>(gs[j], u[j], cutoff));
+        }
+        __syncthreads();   // red[] is rewritten by the next row
+    }
+}
+
 // ------------------------------------------------------------ scalar rows
 // Any layout: one CTA per row, one element per access; each pass re-reads
 // the gate (from L1/L2 after the first pass).
@@ -1307,6 +1380,27 @@ CtaFn cta_fn(int nt, int v, int cluster, int dtype, bool native) {
     }
 }
 
+// Split rows: NT threads of 8 gate vectors, U slice vectors per thread.
+template <class F>
+CtaFn split_fn_f(int nt, int u) {
+    switch (nt * 8 + u) {
+    case 256 * 8 + 1: return gelu_split_rows<256, 8, 1, F>;
+    case 256 * 8 + 2: return gelu_split_rows<256, 8, 2, F>;
+    case 256 * 8 + 4: return gelu_split_rows<256, 8, 4, F>;
+    case 512 * 8 + 1: return gelu_split_rows<512, 8, 1, F>;
+    case 512 * 8 + 2: return gelu_split_rows<512, 8, 2, F>;
+    case 512 * 8 + 4: return gelu_split_rows<512, 8, 4, F>;
+    default: return nullptr;
+    }
+}
+CtaFn split_fn(int nt, int u, int dtype) {
+    switch (dtype) {
+    case GATED_ACT_F16: return split_fn_f<FmtF16>(nt, u);
+    case GATED_ACT_F32: return split_fn_f<FmtF32>(nt, u);
+    default: return split_fn_f<FmtBf16>(nt, u);
+    }
+}
+
 ScalarFn scalar_fn(int dtype, bool native) {
     switch (dtype) {
     case GATED_ACT_F16:
@@ -1356,7 +1450,8 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 struct Plan {
     gated_act_plan pub;
-    int sv;        // vectors per CTA slice (CTA rows)
+    int sv;        // vectors per CTA slice (CTA rows, split rows)
+    int su;        // slice vectors per thread (split rows)
     int dtype;     // gated_act_dtype of in and out
     bool native;   // native-rounding composition
 };
@@ -1506,7 +1601,7 @@ int make_plan(const void *out, const void *in, int64_t T, int64_t d, int64_t rs,
     const int rc = validate(out, in, T, d, rs, elem, check_ptrs);
     if (rc != GATED_ACT_OK)
         return rc;
-    if (variant < GATED_ACT_VARIANT_AUTO || variant > GATED_ACT_VARIANT_PIPE_ROWS)
+    if (variant < GATED_ACT_VARIANT_AUTO || variant > GATED_ACT_VARIANT_SPLIT_ROWS)
         return GATED_ACT_ERR_VARIANT;
     const bool forced = variant != GATED_ACT_VARIANT_AUTO;
     // the warp-rows and bulk-copy kernels exist for plain bf16 only; bulk
@@ -1517,9 +1612,14 @@ int make_plan(const void *out, const void *in, int64_t T, int64_t d, int64_t rs,
         return GATED_ACT_ERR_VARIANT;
     if (host_mem && bulk)
         return GATED_ACT_ERR_VARIANT;
+    // split rows read the gate half-row once per CTA: not from host memory,
+    // and not in native mode
+    if (variant == GATED_ACT_VARIANT_SPLIT_ROWS && (native || host_mem))
+        return GATED_ACT_ERR_VARIANT;
     gated_act_plan &q = p->pub;
     q = gated_act_plan{};
     p->sv = 0;
+    p->su = 0;
     p->dtype = dtype;
     p->native = native;
     const bool vec_ok = aligned(in, 16) && aligned(out, 16) && d % epv == 0 && rs % epv == 0;
@@ -1552,6 +1652,26 @@ int make_plan(const void *out, const void *in, int64_t T, int64_t d, int64_t rs,
     //  * tma rows for the widest rows at many rows per SM;
     //  * one CTA per row everywhere else, except up to 64 rows wider than
     //    8192, where clusters put more SMs on each row.
+    // Split rows, measured on GB300 against cluster rows and one CTA per row
+    // at T = 9 ... 192: while all CTAs fit one wave, from 9 rows of d = 16384
+    // (the most CTAs per row of 8, 4, 2 that fit: 16 rows 2.69 us against
+    // 2.93 in 8-CTA clusters; 32 rows 2.98 against 3.30; 64 rows 3.49
+    // against 3.66 with one CTA per row) and from 33 rows of wider rows up
+    // to d = 32768, two CTAs per row (64 x 32768: 4.65 against 5.15 us in
+    // 2-CTA clusters; 64 x 20480: 3.83 against 4.29).  At 9-32 rows of the
+    // wider rows 4-CTA clusters stay ahead, and at 80 rows and more (two
+    // waves) one CTA per row.
+    int split_c = 0;
+    if (vec_ok && !native && !host_mem && T > kFewRows && nvec >= 2048 && nvec <= 4096) {
+        if (nvec == 2048) {
+            for (int c = kMaxCluster; c >= 2 && !split_c; c /= 2)
+                if (T * c <= sms)
+                    split_c = c;
+        } else if (T > 4 * kFewRows && 2 * T <= sms) {
+            split_c = 2;
+        }
+    }
+
     if (variant == GATED_ACT_VARIANT_AUTO) {
         const int64_t sm = static_cast<int64_t>(sms);
         if (!vec_ok || nvec > int64_t(kMaxSliceVec) * kMaxCluster)
@@ -1565,9 +1685,33 @@ int make_plan(const void *out, const void *in, int64_t T, int64_t d, int64_t rs,
             variant = GATED_ACT_VARIANT_TMA_ROWS;
         else if (nvec <= 64 && !cta_only)
             variant = GATED_ACT_VARIANT_WARP_ROWS;
+        else if (split_c > 0)
+            variant = GATED_ACT_VARIANT_SPLIT_ROWS;
         else
             variant = GATED_ACT_VARIANT_CTA_ROW;
-        cluster = 0;
+        cluster = variant == GATED_ACT_VARIANT_SPLIT_ROWS ? split_c : 0;
+    }
+
+    if (variant == GATED_ACT_VARIANT_SPLIT_ROWS) {
+        // C CTAs per row (2, 4 or 8), 8 gate vectors per thread for the whole
+        // row: 256 threads up to 2048 vectors, 512 up to 4096
+        const int C = cluster;
+        if (!vec_ok || (C != 2 && C != 4 && C != 8) || nvec > 4096)
+            return GATED_ACT_ERR_VARIANT;
+        const int nt = nvec <= 2048 ? 256 : 512;
+        const int64_t sv = ceil_div(nvec, C);
+        const int su = pow2_ceil(ceil_div(sv, nt));
+        if (su > 4)
+            return GATED_ACT_ERR_VARIANT;
+        q.variant = variant;
+        q.cluster = C;
+        q.threads = nt;
+        q.vec_per_thread = 8;
+        q.rows_per_cta = 1;
+        q.grid = std::min<int64_t>(T, 0x7FFFFFFF / C) * C;
+        p->sv = static_cast<int>(sv);
+        p->su = su;
+        return GATED_ACT_OK;
     }
 
     if (variant == GATED_ACT_VARIANT_TMA_ROWS) {
@@ -1819,6 +1963,14 @@ int launch(const Plan &p, void *out, const void *in, int64_t T, int64_t d, int64
     case GATED_ACT_VARIANT_WARP_ROWS:
         e = launch_kernel(warp_fn(q.vec_per_thread), grid, block, 0, stream, 1, o, x, T, di, rs, zf);
         break;
+    case GATED_ACT_VARIANT_SPLIT_ROWS: {
+        CtaFn fn = split_fn(q.threads, p.su, p.dtype);
+        if (!fn)
+            return GATED_ACT_ERR_VARIANT;
+        e = launch_kernel(fn, grid, block, 0, stream, 1, out, in, T, di, rs, zf,
+                          static_cast<int>(q.cluster), p.sv);
+        break;
+    }
     case GATED_ACT_VARIANT_CTA_ROW: {
         CtaFn fn = cta_fn(q.threads, q.vec_per_thread, q.cluster, p.dtype, p.native);
         if (!fn)

@@ -198,14 +198,20 @@ typedef enum gated_act_variant {
     GATED_ACT_VARIANT_SCALAR = 3,    /* any layout: one CTA per row, 2-byte loads   */
     GATED_ACT_VARIANT_TMA_ROWS = 4,  /* persistent CTAs; gate/up half-rows stream
                                         through shared memory by bulk copy          */
-    GATED_ACT_VARIANT_PIPE_ROWS = 5  /* as TMA_ROWS, with one producer lane that
+    GATED_ACT_VARIANT_PIPE_ROWS = 5, /* as TMA_ROWS, with one producer lane that
                                         issues the copies and picks rows while the
                                         other warps finish rows                      */
+    GATED_ACT_VARIANT_SPLIT_ROWS = 6 /* a few wide rows: C = 2, 4 or 8 independent
+                                        CTAs per row, each reading the whole gate
+                                        half-row for the statistics and finishing
+                                        1/C of the columns (device memory, plain
+                                        mode, rows of up to 4096 16-byte vectors) */
 } gated_act_variant;
 
 typedef struct gated_act_plan {
     int32_t variant;        /* gated_act_variant actually used                */
-    int32_t cluster;        /* CTAs that share one row (1 = none)             */
+    int32_t cluster;        /* CTAs that share one row (1 = none): a cluster in
+                               CTA_ROW, independent CTAs in SPLIT_ROWS          */
     int32_t threads;        /* threads per CTA                                 */
     int32_t vec_per_thread; /* 16-byte vectors of gate per thread (0: scalar)  */
     int32_t rows_per_cta;   /* rows one CTA handles at a time                  */

@@ -177,15 +177,21 @@ def test_plan_geometry_families(lib):
     for T in (9, 16, 32):
         rc, p = plan(lib, T, 32768)
         assert rc == 0 and p["variant"] == "cta_row" and p["cluster"] == 4, T
-    # 33 to 64 rows of d >= 32768: 2-CTA clusters; from 65 rows one CTA per row
-    for T in (33, 48, 64):
+    # 33 rows of d > 16384 and more, while two CTAs per row fit one wave:
+    # split rows, two independent CTAs per row; beyond, one CTA per row
+    for T in (33, 48, 64, 76):
         rc, p = plan(lib, T, 32768)
-        assert rc == 0 and p["variant"] == "cta_row" and p["cluster"] == 2, T
-        assert p["grid"] == 2 * T and p["threads"] == 512
-    assert plan(lib, 65, 32768)[1]["cluster"] == 1
-    assert plan(lib, 16, 16384)[1]["cluster"] == 8      # up to 32 rows of d = 16384
-    assert plan(lib, 40, 16384)[1]["cluster"] == 1
-    assert plan(lib, 64, 16384)[1]["cluster"] == 1
+        assert rc == 0 and p["variant"] == "split_rows" and p["cluster"] == 2, T
+        assert p["grid"] == 2 * T and p["threads"] == 512 and p["vec_per_thread"] == 8
+    assert plan(lib, 77, 32768)[1]["variant"] == "cta_row"
+    assert plan(lib, 77, 32768)[1]["cluster"] == 1
+    # d = 16384 from 9 rows: split rows with the most CTAs per row (8, 4, 2)
+    # that fit one wave of the SMs
+    for T, c in ((9, 8), (19, 8), (20, 4), (38, 4), (39, 2), (64, 2), (76, 2)):
+        rc, p = plan(lib, T, 16384)
+        assert rc == 0 and p["variant"] == "split_rows" and p["cluster"] == c, (T, p)
+        assert p["threads"] == 256 and p["grid"] == c * T
+    assert plan(lib, 77, 16384)[1]["variant"] == "cta_row"
     # rows wider than one CTA's registers are split across a cluster
     rc, p = plan(lib, 2048, 65536, variant=ga.VARIANT_CTA_ROW)
     assert rc == 0 and p["cluster"] == 2 and p["grid"] == 4096
@@ -214,6 +220,10 @@ def test_plan_covers_every_slice(lib):
                 assert p["threads"] * p["vec_per_thread"] >= sv
                 assert p["threads"] <= 1024 and p["cluster"] <= 8
                 assert p["grid"] % p["cluster"] == 0
+            elif p["variant"] == "split_rows":
+                # every CTA holds the whole row's gate for the statistics
+                assert p["threads"] * p["vec_per_thread"] >= nvec
+                assert p["cluster"] in (2, 4, 8) and p["grid"] == T * p["cluster"]
             else:
                 pytest.fail(f"aligned d={d} fell back to scalar")
 
@@ -229,12 +239,10 @@ def test_plan_eight_cta_clusters_use_two_vector_slices(lib):
     assert rc == 0 and p["cluster"] == 4 and p["vec_per_thread"] == 4
     # d = 16384: 8-CTA clusters of 128 two-vector threads up to 32 rows, then
     # one CTA per row
-    for T in (1, 8, 9, 16, 32):
+    for T in (1, 8):
         rc, p = plan(lib, T, 16384)
-        assert rc == 0 and p["cluster"] == 8 and p["threads"] == 128, (T, p)
-    for T in (33, 64):
-        rc, p = plan(lib, T, 16384)
-        assert rc == 0 and p["cluster"] == 1, (T, p)
+        assert rc == 0 and p["variant"] == "cta_row" and p["cluster"] == 8
+        assert p["threads"] == 128, (T, p)
     # above 8192 up to 16384: 8-CTA clusters up to 8 rows, 16 rows, and 32
     # rows from 14336
     for T, d, c in ((8, 8192, 1), (1, 9216, 8), (8, 9216, 8), (16, 11008, 8), (17, 11008, 1),
@@ -247,12 +255,32 @@ def test_plan_eight_cta_clusters_use_two_vector_slices(lib):
     assert plan(lib, 1215, 28672)[1]["variant"] == "pipe_rows"
     assert plan(lib, 2048, 28672, ws=1)[1]["variant"] == "pipe_rows"
     # between 16384 and 32768: 8-CTA clusters up to 8 rows, 4-CTA clusters to
-    # 32, 2-CTA clusters to 64
+    # 32, then split rows of two CTAs while they fit one wave
     for d in (20480, 24576):
         assert plan(lib, 8, d)[1]["cluster"] == 8
         assert plan(lib, 16, d)[1]["cluster"] == 4
+        assert plan(lib, 33, d)[1]["variant"] == "split_rows"
         assert plan(lib, 33, d)[1]["cluster"] == 2
-        assert plan(lib, 65, d)[1]["cluster"] == 1
+        assert plan(lib, 77, d)[1]["cluster"] == 1
+
+
+def test_plan_split_rows_forced_and_refused(lib):
+    # forced: any C of 2, 4, 8 for rows of up to 4096 vectors
+    for d, c, nt in ((1024, 2, 256), (16384, 4, 256), (16392, 8, 512), (32768, 2, 512)):
+        rc, p = plan(lib, 5, d, variant=ga.VARIANT_SPLIT_ROWS, cluster=c)
+        assert rc == 0 and p["variant"] == "split_rows" and p["cluster"] == c, (d, p)
+        assert p["threads"] == nt and p["grid"] == 5 * c
+    for d, c in ((16384, 0), (16384, 3), (16384, 16), (32776, 2), (16384 + 4, 2)):
+        assert plan(lib, 5, d, variant=ga.VARIANT_SPLIT_ROWS, cluster=c)[0] == ga.ERR_VARIANT
+    # native mode keeps cluster rows; split rows are refused there
+    p = ga.Plan()
+    assert lib.gelu_and_mul_sparse_native_plan(0x10000, 0x100000, 16, 16384, 32768, ga.BF16, 0,
+                                               ctypes.byref(p)) == ga.OK
+    assert p.variant == ga.VARIANT_CTA_ROW and p.cluster > 1
+    # fp16 rows of the same width take split rows too; fp32 rows of 8192
+    # (the same 2048 vectors) as well
+    assert plan(lib, 16, 16384, dtype=ga.F16)[1]["variant"] == "split_rows"
+    assert plan(lib, 16, 8192, dtype=ga.F32)[1]["variant"] == "split_rows"
 
 
 def test_plan_falls_back_to_scalar(lib):

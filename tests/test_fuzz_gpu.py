@@ -62,6 +62,8 @@ def draw(i: int, variants=(0, 0, 0, 1, 2, 2, 3, 4, 4), seed0: int = 20_000) -> d
         cluster = int(r.choice([0, 1, 2, 4, 8, 16]))
     elif variant == 5:
         cluster = int(r.choice([0, 0, 1, 2, 4, 8]))
+    elif variant == 6:
+        cluster = int(r.choice([2, 4, 8]))
     return {"dtype": dt, "T": T, "d": d, "rs": 2 * d + pad, "z": z, "variant": variant,
             "cluster": cluster, "ws": bool(r.random() < 0.5), "const_row": bool(r.random() < 0.5),
             "seed": 30_000 + i}
@@ -85,6 +87,15 @@ N_PIPE = 80 * SCALE
 @pytest.mark.parametrize("i", range(N_PIPE))
 def test_random_pipe_launch(ga, oracle, i):
     run_case(ga, oracle, draw(i, variants=(5, 5, 5, 0), seed0=90_000), f"pipe case {i}")
+
+
+# split rows forced (or the library's choice)
+N_SPLIT = 60 * SCALE
+
+
+@pytest.mark.parametrize("i", range(N_SPLIT))
+def test_random_split_launch(ga, oracle, i):
+    run_case(ga, oracle, draw(i, variants=(6, 6, 6, 0), seed0=120_000), f"split case {i}")
 
 
 def run_case(ga, oracle, c: dict, name: str):

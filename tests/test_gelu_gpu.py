@@ -59,21 +59,49 @@ def test_decode_forced_clusters(ga, oracle, cluster):
     check_gelu(out, inp.x, inp.d, res, f"decode16 c{cluster}")
 
 
-# few rows wider than 8192 that the plan spreads over clusters: 8-CTA
-# clusters (up to 8 rows, 16 up to d = 16384, 32 from d = 14336), the first
-# counts past those rules, and rows between 16384 and 32768 wide in 4- and
-# 2-CTA clusters (rows = T random rows + 3 constant rows)
-@pytest.mark.parametrize("rows,d,cluster", [(9, 16384, 8), (16, 16384, 8), (24, 16384, 8),
-                                            (32, 16384, 8), (33, 16384, 1), (16, 20480, 4),
-                                            (32, 24576, 4), (48, 24576, 2), (4, 9216, 8),
-                                            (16, 11008, 8), (17, 11008, 1), (24, 14336, 8)])
-def test_wide_few_rows_in_clusters(ga, oracle, rows, d, cluster):
+# few rows wider than 8192 that the plan spreads over several CTAs: 8-CTA
+# clusters (up to 8 rows, 16 up to d = 16384, 32 from d = 14336), 4-CTA
+# clusters for up to 32 rows wider than 16384, and split rows (independent
+# CTAs, each with the whole row's statistics) from 9 rows of d = 16384 and
+# from 33 rows wider than that, while they fit one wave (rows = T random rows
+# + 3 constant rows)
+@pytest.mark.parametrize("rows,d,variant,cluster", [
+    (4, 16384, "cta_row", 8), (9, 16384, "split_rows", 8), (16, 16384, "split_rows", 8),
+    (24, 16384, "split_rows", 4), (33, 16384, "split_rows", 4), (64, 16384, "split_rows", 2),
+    (80, 16384, "cta_row", 1), (16, 20480, "cta_row", 4), (32, 24576, "cta_row", 4),
+    (48, 24576, "split_rows", 2), (70, 32768, "split_rows", 2), (4, 9216, "cta_row", 8),
+    (16, 11008, "cta_row", 8), (17, 11008, "cta_row", 1), (24, 14336, "cta_row", 8)])
+def test_wide_few_rows_spread_over_ctas(ga, oracle, rows, d, variant, cluster):
     inp = W.sweep(rows - 3, d, z=W.Z95, const_rows=True)
     assert inp.x.shape[0] == rows
     plan = ga.gelu_and_mul_sparse_plan(inp.x.cuda(), d=inp.d)
-    assert plan["variant"] == "cta_row" and plan["cluster"] == cluster, plan
+    assert plan["variant"] == variant and plan["cluster"] == cluster, plan
     res = oracle_of(oracle, inp.x, inp.d, inp.z)
-    check_gelu(run(ga, inp.x, inp.d, inp.z), inp.x, inp.d, res, f"{inp.name} plan c{cluster}")
+    out = run(ga, inp.x, inp.d, inp.z)
+    check_gelu(out, inp.x, inp.d, res, f"{inp.name} {variant} c{cluster}")
+    assert torch.count_nonzero(out[-3:].float()).item() == 0
+
+
+# split rows forced: every CTA count, ragged widths (the last slice short or
+# empty), fp16 and fp32 rows, strided rows with NaN in the padding
+@pytest.mark.parametrize("T,d,c,dtype,pad", [
+    (5, 16384, 2, torch.bfloat16, 0), (7, 16384, 4, torch.bfloat16, 0),
+    (3, 16384, 8, torch.bfloat16, 0), (6, 32768, 8, torch.bfloat16, 0),
+    (4, 16392, 8, torch.bfloat16, 0), (9, 1000, 8, torch.bfloat16, 0),
+    (11, 8, 2, torch.bfloat16, 0), (6, 16384, 4, torch.float16, 0),
+    (6, 8192, 8, torch.float32, 0), (5, 12296, 4, torch.bfloat16, 24)])
+def test_split_rows_forced(ga, oracle, T, d, c, dtype, pad):
+    inp = W.iid(T, d, seed=T * 7 + d + c, row_stride=2 * d + pad, dtype=dtype)
+    x = inp.x.clone()
+    if pad:
+        x[:, 2 * d:] = float("nan")
+    out = ga.gelu_and_mul_sparse(x.cuda(), inp.z, d=d, variant=ga.VARIANT_SPLIT_ROWS, cluster=c)
+    torch.cuda.synchronize()
+    if dtype == torch.bfloat16:
+        res = oracle.gelu_and_mul_sparse(W.to_bits(x), d=d, z=inp.z)
+    else:
+        res = oracle.gelu_and_mul_sparse_typed(x.contiguous().numpy(), d=d, z=inp.z)
+    check_gelu(out.cpu(), x, d, res, f"split T{T} d{d} c{c} {dtype}")
 
 
 # many rows of d = 28672 without a workspace: tma rows (round-robin rows)
