@@ -286,6 +286,8 @@ def kernel_name(plan: dict) -> str:
         return f"gelu_tma_rows<{plan['threads']},4>"
     if v == "pipe_rows":
         return f"gelu_pipe_rows<{plan['threads'] // 32 - 1},{plan['vec_per_thread']}>"
+    if v == "split_rows":
+        return f"gelu_split_rows<{plan['threads']},{plan['vec_per_thread']}> x{plan['cluster']}"
     return v
 
 

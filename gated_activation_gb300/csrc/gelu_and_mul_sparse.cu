@@ -1653,18 +1653,20 @@ int make_plan(const void *out, const void *in, int64_t T, int64_t d, int64_t rs,
     //  * one CTA per row everywhere else, except up to 64 rows wider than
     //    8192, where clusters put more SMs on each row.
     // Split rows, measured on GB300 against cluster rows and one CTA per row
-    // at T = 9 ... 192: while all CTAs fit one wave, from 9 rows of d = 16384
-    // (the most CTAs per row of 8, 4, 2 that fit: 16 rows 2.69 us against
-    // 2.93 in 8-CTA clusters; 32 rows 2.98 against 3.30; 64 rows 3.49
-    // against 3.66 with one CTA per row) and from 33 rows of wider rows up
-    // to d = 32768, two CTAs per row (64 x 32768: 4.65 against 5.15 us in
-    // 2-CTA clusters; 64 x 20480: 3.83 against 4.29).  At 9-32 rows of the
-    // wider rows 4-CTA clusters stay ahead, and at 80 rows and more (two
-    // waves) one CTA per row.
+    // at T = 9 ... 192 and d = 4096 ... 32768: from 9 rows of 8192 < d <=
+    // 16384 with the most CTAs per row of 8, 4, 2 that fit one wave (16 rows:
+    // 2.56 against 2.92 us in 8-CTA clusters at d = 16384, 2.42 against 2.89
+    // at d = 11008; 64 rows 3.49 against 3.66 with one CTA per row at d =
+    // 16384), at d = 8192 only with 8 or 4 CTAs per row (2-5% ahead; two lose
+    // to one CTA of 512 threads), and from 33 rows of wider rows up to
+    // d = 32768 with two CTAs per row (64 x 32768: 4.51 against 5.14 us in
+    // 2-CTA clusters).  At 9-32 rows of the wider rows 4-CTA clusters stay
+    // ahead, beyond one wave one CTA per row, and at d = 4096 split rows lose.
     int split_c = 0;
-    if (vec_ok && !native && !host_mem && T > kFewRows && nvec >= 2048 && nvec <= 4096) {
-        if (nvec == 2048) {
-            for (int c = kMaxCluster; c >= 2 && !split_c; c /= 2)
+    if (vec_ok && !native && !host_mem && T > kFewRows && nvec >= 1024 && nvec <= 4096) {
+        if (nvec <= 2048) {
+            const int cmin = nvec > 1024 ? 2 : 4;
+            for (int c = kMaxCluster; c >= cmin && !split_c; c /= 2)
                 if (T * c <= sms)
                     split_c = c;
         } else if (T > 4 * kFewRows && 2 * T <= sms) {
