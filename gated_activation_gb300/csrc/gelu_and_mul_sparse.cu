@@ -1653,25 +1653,33 @@ int make_plan(const void *out, const void *in, int64_t T, int64_t d, int64_t rs,
     //  * one CTA per row everywhere else, except up to 64 rows wider than
     //    8192, where clusters put more SMs on each row.
     // Split rows, measured on GB300 against cluster rows and one CTA per row
-    // at T = 9 ... 192 and d = 4096 ... 32768: from 9 rows of 8192 < d <=
-    // 16384 with the most CTAs per row of 8, 4, 2 that fit one wave (16 rows:
-    // 2.56 against 2.92 us in 8-CTA clusters at d = 16384, 2.42 against 2.89
-    // at d = 11008; 64 rows 3.49 against 3.66 with one CTA per row at d =
-    // 16384), at d = 8192 only with 8 or 4 CTAs per row (2-5% ahead; two lose
-    // to one CTA of 512 threads), and from 33 rows of wider rows up to
-    // d = 32768 with two CTAs per row (64 x 32768: 4.51 against 5.14 us in
-    // 2-CTA clusters).  At 9-32 rows of the wider rows 4-CTA clusters stay
-    // ahead, beyond one wave one CTA per row, and at d = 4096 split rows lose.
+    // at T = 1 ... 192 and d = 4096 ... 32768, with the most CTAs per row that
+    // fit one wave:
+    //  * 8192 < d <= 16384, any T: 8, 4 or 2 per row (1 x 16384: 2.03 against
+    //    2.16 us in 8-CTA clusters; 16 x 11008: 2.42 against 2.89; 64 x 16384:
+    //    3.34 against 3.66 with one CTA per row);
+    //  * d = 8192 from 9 rows, 8 or 4 per row only (2-5% ahead; at fewer rows,
+    //    or with two per row, one CTA of 512 threads wins);
+    //  * wider rows up to d = 32768: 8 or 4 per row at 9-32 rows (16 x 32768:
+    //    3.13 against 3.45 in 4-CTA clusters), 2 per row at 33 and more (64 x
+    //    32768: 4.50 against 5.14 in 2-CTA clusters), and at up to 8 rows 8
+    //    per row up to d = 20480 only (at d = 32768 8-CTA clusters stay 4-5%
+    //    ahead);
+    //  * d = 4096, and beyond one wave: split rows lose.
     int split_c = 0;
-    if (vec_ok && !native && !host_mem && T > kFewRows && nvec >= 1024 && nvec <= 4096) {
-        if (nvec <= 2048) {
-            const int cmin = nvec > 1024 ? 2 : 4;
-            for (int c = kMaxCluster; c >= cmin && !split_c; c /= 2)
-                if (T * c <= sms)
-                    split_c = c;
-        } else if (T > 4 * kFewRows && 2 * T <= sms) {
-            split_c = 2;
-        }
+    if (vec_ok && !native && !host_mem && nvec >= 1024 && nvec <= 4096) {
+        int cmin = 2, cmax = kMaxCluster;
+        if (nvec == 1024)
+            cmin = T > kFewRows ? 4 : 2 * kMaxCluster;
+        else if (nvec > 2048 && T <= kFewRows)
+            cmin = nvec <= 2560 ? kMaxCluster : 2 * kMaxCluster;
+        else if (nvec > 2048 && T <= 4 * kFewRows)
+            cmin = 4;
+        else if (nvec > 2048)
+            cmax = 2;
+        for (int c = cmax; c >= cmin && !split_c; c /= 2)
+            if (T * c <= sms)
+                split_c = c;
     }
 
     if (variant == GATED_ACT_VARIANT_AUTO) {

@@ -173,10 +173,10 @@ def test_plan_geometry_families(lib):
     # a handful of wide rows: 8-CTA clusters per row
     rc, p = plan(lib, 1, 32768)
     assert rc == 0 and p["variant"] == "cta_row" and p["cluster"] == 8
-    # 9 to 32 rows of d >= 32768: 4-CTA clusters
-    for T in (9, 16, 32):
+    # 9 to 32 rows of d >= 32768: split rows of 8 (to 19 rows) or 4 CTAs
+    for T, c in ((9, 8), (19, 8), (20, 4), (32, 4)):
         rc, p = plan(lib, T, 32768)
-        assert rc == 0 and p["variant"] == "cta_row" and p["cluster"] == 4, T
+        assert rc == 0 and p["variant"] == "split_rows" and p["cluster"] == c, T
     # 33 rows of d > 16384 and more, while two CTAs per row fit one wave:
     # split rows, two independent CTAs per row; beyond, one CTA per row
     for T in (33, 48, 64, 76):
@@ -185,9 +185,9 @@ def test_plan_geometry_families(lib):
         assert p["grid"] == 2 * T and p["threads"] == 512 and p["vec_per_thread"] == 8
     assert plan(lib, 77, 32768)[1]["variant"] == "cta_row"
     assert plan(lib, 77, 32768)[1]["cluster"] == 1
-    # d = 16384 from 9 rows: split rows with the most CTAs per row (8, 4, 2)
-    # that fit one wave of the SMs
-    for T, c in ((9, 8), (19, 8), (20, 4), (38, 4), (39, 2), (64, 2), (76, 2)):
+    # d = 16384: split rows with the most CTAs per row (8, 4, 2) that fit one
+    # wave of the SMs
+    for T, c in ((1, 8), (8, 8), (9, 8), (19, 8), (20, 4), (38, 4), (39, 2), (64, 2), (76, 2)):
         rc, p = plan(lib, T, 16384)
         assert rc == 0 and p["variant"] == "split_rows" and p["cluster"] == c, (T, p)
         assert p["threads"] == 256 and p["grid"] == c * T
@@ -234,24 +234,22 @@ def test_plan_eight_cta_clusters_use_two_vector_slices(lib):
     for T in (1, 8):
         rc, p = plan(lib, T, 32768)
         assert rc == 0 and p["cluster"] == 8 and p["threads"] == 256 and p["vec_per_thread"] == 2
-    # 4-CTA clusters keep four vectors per thread
-    rc, p = plan(lib, 16, 32768)
+    # 4-CTA clusters (forced) keep four vectors per thread
+    rc, p = plan(lib, 16, 32768, variant=ga.VARIANT_CTA_ROW, cluster=4)
     assert rc == 0 and p["cluster"] == 4 and p["vec_per_thread"] == 4
-    # d = 16384: 8-CTA clusters of 128 two-vector threads up to 32 rows, then
-    # one CTA per row
+    # up to 8 rows of 24576 and more: 8-CTA clusters of two-vector threads
     for T in (1, 8):
-        rc, p = plan(lib, T, 16384)
-        assert rc == 0 and p["variant"] == "cta_row" and p["cluster"] == 8
-        assert p["threads"] == 128, (T, p)
+        rc, p = plan(lib, T, 24576)
+        assert rc == 0 and p["variant"] == "cta_row" and p["cluster"] == 8, (T, p)
     # above 8192 up to 16384: 8-CTA clusters up to 8 rows, 16 rows, and 32
     # rows from 14336
-    for T, d, c in ((8, 8192, 1), (1, 9216, 8), (8, 9216, 8), (8, 14336, 8)):
-        rc, p = plan(lib, T, d)
-        assert rc == 0 and p["variant"] == "cta_row" and p["cluster"] == c, (T, d, p)
-    # from 9 rows above d = 8192: split rows, the most CTAs per row that fit
-    # one wave; at d = 8192 only 8 or 4 of them
-    for T, d, c in ((9, 9216, 8), (16, 11008, 8), (17, 11008, 8), (24, 12288, 4), (38, 14336, 4),
-                    (39, 14336, 2), (76, 9216, 2), (9, 8192, 8), (38, 8192, 4)):
+    rc, p = plan(lib, 8, 8192)
+    assert rc == 0 and p["variant"] == "cta_row" and p["cluster"] == 1
+    # above d = 8192: split rows, the most CTAs per row that fit one wave; at
+    # d = 8192 only 8 or 4 of them, from 9 rows
+    for T, d, c in ((1, 9216, 8), (8, 14336, 8), (9, 9216, 8), (16, 11008, 8), (17, 11008, 8),
+                    (24, 12288, 4), (38, 14336, 4), (39, 14336, 2), (76, 9216, 2), (9, 8192, 8),
+                    (38, 8192, 4), (1, 20480, 8), (8, 20480, 8)):
         rc, p = plan(lib, T, d)
         assert rc == 0 and p["variant"] == "split_rows" and p["cluster"] == c, (T, d, p)
     for T, d in ((39, 8192), (77, 11008), (64, 4096)):
@@ -261,13 +259,12 @@ def test_plan_eight_cta_clusters_use_two_vector_slices(lib):
     assert plan(lib, 1219, 28672)[1]["variant"] == "tma_rows"
     assert plan(lib, 1215, 28672)[1]["variant"] == "pipe_rows"
     assert plan(lib, 2048, 28672, ws=1)[1]["variant"] == "pipe_rows"
-    # between 16384 and 32768: 8-CTA clusters up to 8 rows, 4-CTA clusters to
-    # 32, then split rows of two CTAs while they fit one wave
+    # between 16384 and 32768: split rows of 8 CTAs to 19 rows, of 4 to 32,
+    # of 2 while they fit one wave; then one CTA per row
     for d in (20480, 24576):
-        assert plan(lib, 8, d)[1]["cluster"] == 8
-        assert plan(lib, 16, d)[1]["cluster"] == 4
-        assert plan(lib, 33, d)[1]["variant"] == "split_rows"
-        assert plan(lib, 33, d)[1]["cluster"] == 2
+        for T, c in ((16, 8), (24, 4), (33, 2)):
+            rc, p = plan(lib, T, d)
+            assert rc == 0 and p["variant"] == "split_rows" and p["cluster"] == c, (T, d, p)
         assert plan(lib, 77, d)[1]["cluster"] == 1
 
 

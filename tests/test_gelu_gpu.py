@@ -59,19 +59,19 @@ def test_decode_forced_clusters(ga, oracle, cluster):
     check_gelu(out, inp.x, inp.d, res, f"decode16 c{cluster}")
 
 
-# few wide rows that the plan spreads over several CTAs: 8-CTA clusters (up
-# to 8 rows wider than 8192), 4-CTA clusters for 9-32 rows wider than 16384,
-# and split rows (independent CTAs, each with the whole row's statistics)
-# from 9 rows of 8192 < d <= 16384 (at d = 8192 with 8 or 4 CTAs per row) and
-# from 33 rows wider than that, while they fit one wave (rows = T random
-# rows + 3 constant rows)
+# few wide rows that the plan spreads over several CTAs: split rows
+# (independent CTAs, each with the whole row's statistics) while they fit one
+# wave -- at any row count above d = 8192 up to 20480, from 9 rows at d =
+# 8192 (8 or 4 CTAs per row) and wider -- and 8-CTA clusters for up to 8 rows
+# wider than 20480 (rows = T random rows + 3 constant rows)
 @pytest.mark.parametrize("rows,d,variant,cluster", [
-    (4, 16384, "cta_row", 8), (9, 16384, "split_rows", 8), (16, 16384, "split_rows", 8),
+    (4, 16384, "split_rows", 8), (9, 16384, "split_rows", 8), (16, 16384, "split_rows", 8),
     (24, 16384, "split_rows", 4), (33, 16384, "split_rows", 4), (64, 16384, "split_rows", 2),
-    (80, 16384, "cta_row", 1), (16, 20480, "cta_row", 4), (32, 24576, "cta_row", 4),
-    (48, 24576, "split_rows", 2), (70, 32768, "split_rows", 2), (4, 9216, "cta_row", 8),
+    (80, 16384, "cta_row", 1), (16, 20480, "split_rows", 8), (32, 24576, "split_rows", 4),
+    (48, 24576, "split_rows", 2), (70, 32768, "split_rows", 2), (4, 9216, "split_rows", 8),
     (16, 11008, "split_rows", 8), (24, 14336, "split_rows", 4), (60, 12288, "split_rows", 2),
-    (20, 8192, "split_rows", 4), (40, 8192, "cta_row", 1)])
+    (20, 8192, "split_rows", 4), (40, 8192, "cta_row", 1), (4, 32768, "cta_row", 8),
+    (8, 24576, "cta_row", 8), (12, 32768, "split_rows", 8)])
 def test_wide_few_rows_spread_over_ctas(ga, oracle, rows, d, variant, cluster):
     inp = W.sweep(rows - 3, d, z=W.Z95, const_rows=True)
     assert inp.x.shape[0] == rows
