@@ -1658,8 +1658,9 @@ int make_plan(const void *out, const void *in, int64_t T, int64_t d, int64_t rs,
     //  * 8192 < d <= 16384, any T: 8, 4 or 2 per row (1 x 16384: 2.03 against
     //    2.16 us in 8-CTA clusters; 16 x 11008: 2.42 against 2.89; 64 x 16384:
     //    3.34 against 3.66 with one CTA per row);
-    //  * d = 8192 from 9 rows, 8 or 4 per row only (2-5% ahead; at fewer rows,
-    //    or with two per row, one CTA of 512 threads wins);
+    //  * d = 8192, 8 or 4 per row only (1 x 8192: 1.79 against 1.96 us with
+    //    one CTA of 512 threads; 2-5% ahead from 8 rows on, within 1% at 2
+    //    and 4 rows; with two per row one CTA wins);
     //  * wider rows up to d = 32768: 8 or 4 per row at 9-32 rows (16 x 32768:
     //    3.13 against 3.45 in 4-CTA clusters), 2 per row at 33 and more (64 x
     //    32768: 4.50 against 5.14 in 2-CTA clusters), and at up to 8 rows 8
@@ -1670,7 +1671,7 @@ int make_plan(const void *out, const void *in, int64_t T, int64_t d, int64_t rs,
     if (vec_ok && !native && !host_mem && nvec >= 1024 && nvec <= 4096) {
         int cmin = 2, cmax = kMaxCluster;
         if (nvec == 1024)
-            cmin = T > kFewRows ? 4 : 2 * kMaxCluster;
+            cmin = 4;
         else if (nvec > 2048 && T <= kFewRows)
             cmin = nvec <= 2560 ? kMaxCluster : 2 * kMaxCluster;
         else if (nvec > 2048 && T <= 4 * kFewRows)

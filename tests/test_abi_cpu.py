@@ -243,13 +243,13 @@ def test_plan_eight_cta_clusters_use_two_vector_slices(lib):
         assert rc == 0 and p["variant"] == "cta_row" and p["cluster"] == 8, (T, p)
     # above 8192 up to 16384: 8-CTA clusters up to 8 rows, 16 rows, and 32
     # rows from 14336
-    rc, p = plan(lib, 8, 8192)
+    rc, p = plan(lib, 8, 4096)
     assert rc == 0 and p["variant"] == "cta_row" and p["cluster"] == 1
-    # above d = 8192: split rows, the most CTAs per row that fit one wave; at
-    # d = 8192 only 8 or 4 of them, from 9 rows
+    # from d = 8192: split rows, the most CTAs per row that fit one wave; at
+    # d = 8192 only 8 or 4 of them
     for T, d, c in ((1, 9216, 8), (8, 14336, 8), (9, 9216, 8), (16, 11008, 8), (17, 11008, 8),
                     (24, 12288, 4), (38, 14336, 4), (39, 14336, 2), (76, 9216, 2), (9, 8192, 8),
-                    (38, 8192, 4), (1, 20480, 8), (8, 20480, 8)):
+                    (38, 8192, 4), (1, 20480, 8), (8, 20480, 8), (1, 8192, 8), (8, 8192, 8)):
         rc, p = plan(lib, T, d)
         assert rc == 0 and p["variant"] == "split_rows" and p["cluster"] == c, (T, d, p)
     for T, d in ((39, 8192), (77, 11008), (64, 4096)):
