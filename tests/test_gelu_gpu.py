@@ -244,14 +244,18 @@ def test_guard_bands_untouched(ga, oracle):
         check_gelu(out.cpu(), inp.x, d, oracle_of(oracle, inp.x, d, inp.z), f"guard T{T} d{d} v{v}")
 
 
-def test_nan_poisons_only_its_row(ga, oracle):
-    inp = W.iid(6, 2048, seed=17)
+# the plan's choice at d = 2048, and split rows (each CTA of a row reads the
+# NaN for its statistics, so every slice of the row is NaN)
+@pytest.mark.parametrize("d,kw", [(2048, {}), (16384, {"variant": 6, "cluster": 8}),
+                                  (32768, {"variant": 6, "cluster": 2})])
+def test_nan_poisons_only_its_row(ga, oracle, d, kw):
+    inp = W.iid(6, d, seed=17)
     x = inp.x.clone()
-    x[2, 100] = float("nan")            # in the gate: row 2 all NaN
-    x[4, 2048 + 7] = float("nan")       # in up: one element
-    out = run(ga, x, 2048, inp.z)
-    res = oracle_of(oracle, x, 2048, inp.z)
-    check_gelu(out, x, 2048, res, "nan")
+    x[2, d - 100] = float("nan")        # in the gate (the last slice): row 2 all NaN
+    x[4, d + 7] = float("nan")          # in up: one element
+    out = run(ga, x, d, inp.z, **kw)
+    res = oracle_of(oracle, x, d, inp.z)
+    check_gelu(out, x, d, res, f"nan d{d}")
     o = out.float()
     assert torch.isnan(o[2]).all()
     assert torch.isnan(o[4]).sum().item() <= 1
