@@ -394,7 +394,8 @@ def per_shape_times(ga, launches, dev, peak_gbs, reps=5) -> tuple[list, float]:
                "us": round(t * 1e3, 3), "GBps": round(gbs, 1),
                "frac_of_measured": round(gbs / peak_gbs, 4),
                "frac_of_spec_8TBps": round(gbs / SPEC_HBM_GBS, 4),
-               "x_floor": round(t / floor, 3), "launches_in_graph": N}
+               "x_floor": round(t / floor, 3), "launches_in_graph": N,
+               "rows_per_s": round(L.get("live", T) / (t * 1e-3), 1)}
         if "live" in L:
             row["live_rows"] = L["live"]
         if L["op"] in ("gelu", "silu"):
