@@ -32,7 +32,8 @@ def oracle_of(oracle, x_cpu, d, z):
     return oracle.gelu_and_mul_sparse(W.to_bits(x_cpu.contiguous()), d=d, z=z)
 
 
-GEOMETRIES = [(0, 0), (1, 0), (2, 1), (2, 2), (2, 4), (2, 8), (3, 0), (4, 0), (5, 0), (5, 1)]
+GEOMETRIES = [(0, 0), (1, 0), (2, 1), (2, 2), (2, 4), (2, 8), (3, 0), (4, 0), (5, 0), (5, 1),
+              (6, 2), (6, 4), (6, 8)]
 
 
 @pytest.mark.parametrize("variant,cluster", GEOMETRIES)
@@ -51,12 +52,14 @@ def test_decode(ga, oracle, T):
     check_gelu(out, inp.x, inp.d, res, inp.name)
 
 
-@pytest.mark.parametrize("cluster", [1, 2, 4, 8])
-def test_decode_forced_clusters(ga, oracle, cluster):
+@pytest.mark.parametrize("variant,cluster", [(2, 1), (2, 2), (2, 4), (2, 8), (6, 2), (6, 4),
+                                             (6, 8)])
+def test_decode_forced_clusters(ga, oracle, variant, cluster):
+    # the decode workload (outliers in the gate) in clusters and in split rows
     inp = W.decode(16)
     res = oracle_of(oracle, inp.x, inp.d, inp.z)
-    out = run(ga, inp.x, inp.d, inp.z, variant=2, cluster=cluster)
-    check_gelu(out, inp.x, inp.d, res, f"decode16 c{cluster}")
+    out = run(ga, inp.x, inp.d, inp.z, variant=variant, cluster=cluster)
+    check_gelu(out, inp.x, inp.d, res, f"decode16 v{variant} c{cluster}")
 
 
 # few wide rows that the plan spreads over several CTAs: split rows
