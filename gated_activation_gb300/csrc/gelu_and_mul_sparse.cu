@@ -1202,8 +1202,9 @@ gelu_cta_rows(void *__restrict__ out_, const void *__restrict__ in_, int64_t T, 
 // the cluster exchange (0.6-1.2 us per row) from 9 rows on while all CTAs fit
 // one wave.  Thread t holds gate vectors t + NT i (i < V, the whole row) for
 // the statistics and, for the epilogue, the slice's vectors v0 + t + NT j
-// (j < U) of gate and up.
-template <int NT, int V, int U, class F>
+// (j < U) of gate and up.  NATIVE: the native-rounding composition (cutoff
+// and epilogue rounded to the format after every op, a from the table).
+template <int NT, int V, int U, class F, bool NATIVE>
 __global__ void __launch_bounds__(NT, 1)
 gelu_split_rows(void *__restrict__ out_, const void *__restrict__ in_, int64_t T, int d,
                 int64_t rs, float z, int C, int sv) {
@@ -1217,6 +1218,9 @@ gelu_split_rows(void *__restrict__ out_, const void *__restrict__ in_, int64_t T
     const int64_t rs_bytes = rs * F::kElem, d_bytes = static_cast<int64_t>(d) * F::kElem;
     pdl_wait();
     pdl_trigger();
+    const uint16_t *lut = nullptr;   // native mode: the table of a, once built
+    if constexpr (NATIVE)
+        lut = native_table<F>();
     for (int64_t b = blockIdx.x; b < T * C; b += gridDim.x) {
         const int64_t row = b / C;
         const int v0 = static_cast<int>(b - row * C) * sv;
@@ -1253,13 +1257,18 @@ gelu_split_rows(void *__restrict__ out_, const void *__restrict__ in_, int64_t T
                 acc = ssd_vec<F>(acc, g[i], m2);
         const float var =
             __fdiv_rn(block_sum<NW>(acc.x + acc.y, red[1], lane, warp), static_cast<float>(d));
-        const float cutoff = fmaf(__fsqrt_rn(var), z, mean);
+        const float cutoff =
+            NATIVE ? native_cutoff<F>(mean, var, z) : fmaf(__fsqrt_rn(var), z, mean);
         uint8_t *op = out + row * d_bytes;
 #pragma unroll
         for (int j = 0; j < U; ++j) {
             const int v = v0 + tid + NT * j;
-            if (v < v1)
-                st_vec(op + 16 * v, epi_vec<F>(gs[j], u[j], cutoff));
+            if (v < v1) {
+                if constexpr (NATIVE)
+                    st_vec_out(op + 16 * v, epi_vec_native<F>(gs[j], u[j], cutoff, lut));
+                else
+                    st_vec(op + 16 * v, epi_vec<F>(gs[j], u[j], cutoff));
+            }
         }
         __syncthreads();   // red[] is rewritten by the next row
     }
@@ -1381,23 +1390,26 @@ CtaFn cta_fn(int nt, int v, int cluster, int dtype, bool native) {
 }
 
 // Split rows: NT threads of 8 gate vectors, U slice vectors per thread.
-template <class F>
+template <class F, bool N>
 CtaFn split_fn_f(int nt, int u) {
     switch (nt * 8 + u) {
-    case 256 * 8 + 1: return gelu_split_rows<256, 8, 1, F>;
-    case 256 * 8 + 2: return gelu_split_rows<256, 8, 2, F>;
-    case 256 * 8 + 4: return gelu_split_rows<256, 8, 4, F>;
-    case 512 * 8 + 1: return gelu_split_rows<512, 8, 1, F>;
-    case 512 * 8 + 2: return gelu_split_rows<512, 8, 2, F>;
-    case 512 * 8 + 4: return gelu_split_rows<512, 8, 4, F>;
+    case 256 * 8 + 1: return gelu_split_rows<256, 8, 1, F, N>;
+    case 256 * 8 + 2: return gelu_split_rows<256, 8, 2, F, N>;
+    case 256 * 8 + 4: return gelu_split_rows<256, 8, 4, F, N>;
+    case 512 * 8 + 1: return gelu_split_rows<512, 8, 1, F, N>;
+    case 512 * 8 + 2: return gelu_split_rows<512, 8, 2, F, N>;
+    case 512 * 8 + 4: return gelu_split_rows<512, 8, 4, F, N>;
     default: return nullptr;
     }
 }
-CtaFn split_fn(int nt, int u, int dtype) {
+// native: the native-rounding composition (bf16 and fp16 only)
+CtaFn split_fn(int nt, int u, int dtype, bool native) {
     switch (dtype) {
-    case GATED_ACT_F16: return split_fn_f<FmtF16>(nt, u);
-    case GATED_ACT_F32: return split_fn_f<FmtF32>(nt, u);
-    default: return split_fn_f<FmtBf16>(nt, u);
+    case GATED_ACT_F16:
+        return native ? split_fn_f<FmtF16, true>(nt, u) : split_fn_f<FmtF16, false>(nt, u);
+    case GATED_ACT_F32: return native ? nullptr : split_fn_f<FmtF32, false>(nt, u);
+    default:
+        return native ? split_fn_f<FmtBf16, true>(nt, u) : split_fn_f<FmtBf16, false>(nt, u);
     }
 }
 
@@ -1612,9 +1624,8 @@ int make_plan(const void *out, const void *in, int64_t T, int64_t d, int64_t rs,
         return GATED_ACT_ERR_VARIANT;
     if (host_mem && bulk)
         return GATED_ACT_ERR_VARIANT;
-    // split rows read the gate half-row once per CTA: not from host memory,
-    // and not in native mode
-    if (variant == GATED_ACT_VARIANT_SPLIT_ROWS && (native || host_mem))
+    // split rows read the gate half-row once per CTA: not from host memory
+    if (variant == GATED_ACT_VARIANT_SPLIT_ROWS && host_mem)
         return GATED_ACT_ERR_VARIANT;
     gated_act_plan &q = p->pub;
     q = gated_act_plan{};
@@ -1667,17 +1678,24 @@ int make_plan(const void *out, const void *in, int64_t T, int64_t d, int64_t rs,
     //    per row up to d = 20480 only (at d = 32768 8-CTA clusters stay 4-5%
     //    ahead);
     //  * d = 4096, and beyond one wave: split rows lose.
+    // Native rounding (the table-read epilogue) gains more from split rows
+    // (1 x 16384: 2.61 against 3.47 us in 8-CTA clusters; 64 x 32768: 5.62
+    // against 6.78) but keeps one CTA per row where two or four CTAs per row
+    // of d <= 16384 would take it (64 x 16384: 4.01 against 4.46 split in two)
+    // -- at d = 8192 it takes 8 per row only.
     int split_c = 0;
-    if (vec_ok && !native && !host_mem && nvec >= 1024 && nvec <= 4096) {
+    if (vec_ok && !host_mem && nvec >= 1024 && nvec <= 4096) {
         int cmin = 2, cmax = kMaxCluster;
         if (nvec == 1024)
-            cmin = 4;
+            cmin = native ? kMaxCluster : 4;
         else if (nvec > 2048 && T <= kFewRows)
             cmin = nvec <= 2560 ? kMaxCluster : 2 * kMaxCluster;
         else if (nvec > 2048 && T <= 4 * kFewRows)
             cmin = 4;
         else if (nvec > 2048)
             cmax = 2;
+        else if (native)
+            cmin = 4;
         for (int c = cmax; c >= cmin && !split_c; c /= 2)
             if (T * c <= sms)
                 split_c = c;
@@ -1975,7 +1993,7 @@ int launch(const Plan &p, void *out, const void *in, int64_t T, int64_t d, int64
         e = launch_kernel(warp_fn(q.vec_per_thread), grid, block, 0, stream, 1, o, x, T, di, rs, zf);
         break;
     case GATED_ACT_VARIANT_SPLIT_ROWS: {
-        CtaFn fn = split_fn(q.threads, p.su, p.dtype);
+        CtaFn fn = split_fn(q.threads, p.su, p.dtype, p.native);
         if (!fn)
             return GATED_ACT_ERR_VARIANT;
         e = launch_kernel(fn, grid, block, 0, stream, 1, out, in, T, di, rs, zf,

@@ -204,8 +204,8 @@ typedef enum gated_act_variant {
     GATED_ACT_VARIANT_SPLIT_ROWS = 6 /* a few wide rows: C = 2, 4 or 8 independent
                                         CTAs per row, each reading the whole gate
                                         half-row for the statistics and finishing
-                                        1/C of the columns (device memory, plain
-                                        mode, rows of up to 4096 16-byte vectors) */
+                                        1/C of the columns (device memory, rows of
+                                        up to 4096 16-byte vectors)                 */
 } gated_act_variant;
 
 typedef struct gated_act_plan {
@@ -312,8 +312,10 @@ int gelu_and_mul_sparse_typed(void *out, const void *in, int64_t T, int64_t d,
  * element type missing builds it (32768 entries, 64 KB per type, in the
  * library's device memory; that launch computes a directly) and later
  * launches read it through the read-only cache.  Table and direct
- * evaluation give the same bits.  Rows run one CTA (or cluster) per row,
- * the geometry with the most L1 for the table.
+ * evaluation give the same bits.  Rows run one CTA per row (the geometry
+ * with the most L1 for the table), or, for a few wide rows, split over 8 or
+ * 4 CTAs (2 above d = 16384) that each compute the row's statistics, or in
+ * an 8-CTA cluster.
  */
 int gelu_and_mul_sparse_native(void *out, const void *in, int64_t T, int64_t d,
                                int64_t row_stride, double z, int dtype,

@@ -276,11 +276,14 @@ def test_plan_split_rows_forced_and_refused(lib):
         assert p["threads"] == nt and p["grid"] == 5 * c
     for d, c in ((16384, 0), (16384, 3), (16384, 16), (32776, 2), (16384 + 4, 2)):
         assert plan(lib, 5, d, variant=ga.VARIANT_SPLIT_ROWS, cluster=c)[0] == ga.ERR_VARIANT
-    # native mode keeps cluster rows; split rows are refused there
-    p = ga.Plan()
-    assert lib.gelu_and_mul_sparse_native_plan(0x10000, 0x100000, 16, 16384, 32768, ga.BF16, 0,
-                                               ctypes.byref(p)) == ga.OK
-    assert p.variant == ga.VARIANT_CTA_ROW and p.cluster > 1
+    # native mode: split rows of 8 or 4 CTAs, one CTA per row where they
+    # would take two at d <= 16384
+    for T, want in ((16, (ga.VARIANT_SPLIT_ROWS, 8)), (32, (ga.VARIANT_SPLIT_ROWS, 4)),
+                    (64, (ga.VARIANT_CTA_ROW, 1))):
+        p = ga.Plan()
+        assert lib.gelu_and_mul_sparse_native_plan(0x10000, 0x100000, T, 16384, 32768, ga.BF16,
+                                                   GB300_SMS, ctypes.byref(p)) == ga.OK
+        assert (p.variant, p.cluster) == want, (T, p.as_dict())
     # fp16 rows of the same width take split rows too; fp32 rows of 8192
     # (the same 2048 vectors) as well
     assert plan(lib, 16, 16384, dtype=ga.F16)[1]["variant"] == "split_rows"

@@ -54,19 +54,23 @@ def test_native_constant_rows_and_ragged(ga, oracle, dt):
         check_native(run(ga, inp.x, d, inp.z), inp.x, d, ref, mask, cut, f"{dt} d{d}", z=inp.z)
 
 
-# native rows spread over clusters (rows = T random rows + 3 constant rows):
-# 8-CTA clusters for a few rows above d = 8192, 4- and 2-CTA clusters for
-# more rows above 16384
-@pytest.mark.parametrize("rows,d,cluster", [(4, 16384, 8), (16, 14336, 8), (4, 9216, 8),
-                                            (19, 24576, 4), (48, 32768, 2)])
+# native rows spread over several CTAs (rows = T random rows + 3 constant
+# rows): split rows (8 per row for a few rows of d <= 20480 and at d = 8192,
+# 8 or 4 up to 32 rows, 2 beyond for wider rows), 8-CTA clusters for a few
+# rows wider than 20480, one CTA per row where split rows would take two or
+# four at d <= 16384
+@pytest.mark.parametrize("rows,d,variant,cluster", [
+    (4, 16384, "split_rows", 8), (16, 14336, "split_rows", 8), (4, 9216, "split_rows", 8),
+    (19, 24576, "split_rows", 8), (48, 32768, "split_rows", 2), (12, 8192, "split_rows", 8),
+    (4, 32768, "cta_row", 8), (67, 16384, "cta_row", 1)])
 @pytest.mark.parametrize("dt", DTYPES)
-def test_native_cluster_rows(ga, oracle, dt, rows, d, cluster):
+def test_native_rows_over_several_ctas(ga, oracle, dt, rows, d, variant, cluster):
     inp = W.sweep(rows - 3, d, dtype=dt)
     plan = ga.gelu_and_mul_sparse_native_plan(inp.x.cuda(), d=d)
-    assert plan["variant"] == "cta_row" and plan["cluster"] == cluster, plan
+    assert plan["variant"] == variant and plan["cluster"] == cluster, plan
     ref, mask, cut = oracle_native(oracle, inp.x, d, inp.z)
     out = run(ga, inp.x, d, inp.z)
-    check_native(out, inp.x, d, ref, mask, cut, f"{dt} {inp.name} c{cluster}", z=inp.z)
+    check_native(out, inp.x, d, ref, mask, cut, f"{dt} {inp.name} {variant} c{cluster}", z=inp.z)
     assert torch.count_nonzero(out[-3:].float()).item() == 0
 
 
