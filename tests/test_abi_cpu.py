@@ -270,7 +270,8 @@ def test_plan_eight_cta_clusters_use_two_vector_slices(lib):
 
 def test_plan_split_rows_forced_and_refused(lib):
     # forced: any C of 2, 4, 8 for rows of up to 4096 vectors
-    for d, c, nt in ((1024, 2, 256), (16384, 4, 256), (16392, 8, 512), (32768, 2, 512)):
+    for d, c, nt in ((1024, 2, 256), (1024, 8, 128), (8192, 8, 128), (8192, 4, 256),
+                     (16384, 4, 256), (16392, 8, 512), (32768, 2, 512)):
         rc, p = plan(lib, 5, d, variant=ga.VARIANT_SPLIT_ROWS, cluster=c)
         assert rc == 0 and p["variant"] == "split_rows" and p["cluster"] == c, (d, p)
         assert p["threads"] == nt and p["grid"] == 5 * c
