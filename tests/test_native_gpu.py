@@ -99,11 +99,12 @@ def test_native_rejects_fp32(ga):
         ga.gelu_and_mul_sparse_native(x, 1.0)
 
 
-# bf16 native rows at the widest shapes (one CTA, or two-vector CTAs, per
-# row; the plain call takes the bulk-copy geometries here), against the native
-# oracle
+# bf16 native rows at the widest shapes (one CTA per row; the plain call takes
+# the bulk-copy geometries here: pipe rows at all but the last, tma rows
+# there), against the native oracle
 @pytest.mark.parametrize("T,d,threads", [(2048, 16384, 512), (1300, 14336, 512),
-                                         (1024, 32768, 1024)])
+                                         (1024, 32768, 1024), (400, 24576, 1024),
+                                         (1219, 32768, 1024)])
 def test_native_widest_rows(ga, oracle, T, d, threads):
     inp = W.iid(T, d, seed=T + d)
     x = inp.x.cuda()
