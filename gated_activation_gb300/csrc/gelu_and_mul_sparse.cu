@@ -1204,6 +1204,12 @@ gelu_cta_rows(void *__restrict__ out_, const void *__restrict__ in_, int64_t T, 
 // the statistics and, for the epilogue, the slice's vectors v0 + t + NT j
 // (j < U) of gate and up.  NATIVE: the native-rounding composition (cutoff
 // and epilogue rounded to the format after every op, a from the table).
+// The two CTA sums take the narrow butterfly (measured on GB300: 1-3% faster
+// at 1-64 rows of d = 8192 ... 32768; it adds the same partials in the same
+// pairs).  One CTA barrier
+// instead of two -- per-warp two-pass statistics merged in the pairwise form
+// of Chan, Golub and LeVeque -- was 6-12% slower (1 x 8192: 2.15 against
+// 2.03 us; 8 x 20480: 3.03 against 2.73).
 template <int NT, int V, int U, class F, bool NATIVE>
 __global__ void __launch_bounds__(NT, 1)
 gelu_split_rows(void *__restrict__ out_, const void *__restrict__ in_, int64_t T, int d,
@@ -1248,7 +1254,7 @@ gelu_split_rows(void *__restrict__ out_, const void *__restrict__ in_, int64_t T
         for (int i = 0; i < V; ++i)
             acc = sum_vec<F>(acc, g[i]);
         const float mean =
-            __fdiv_rn(block_sum<NW>(acc.x + acc.y, red[0], lane, warp), static_cast<float>(d));
+            __fdiv_rn(block_sum<NW, true>(acc.x + acc.y, red[0], lane, warp), static_cast<float>(d));
         const float2 m2 = make_float2(mean, mean);
         acc = make_float2(0.f, 0.f);
 #pragma unroll
@@ -1256,7 +1262,7 @@ gelu_split_rows(void *__restrict__ out_, const void *__restrict__ in_, int64_t T
             if (tid + NT * i < nvec)
                 acc = ssd_vec<F>(acc, g[i], m2);
         const float var =
-            __fdiv_rn(block_sum<NW>(acc.x + acc.y, red[1], lane, warp), static_cast<float>(d));
+            __fdiv_rn(block_sum<NW, true>(acc.x + acc.y, red[1], lane, warp), static_cast<float>(d));
         const float cutoff =
             NATIVE ? native_cutoff<F>(mean, var, z) : fmaf(__fsqrt_rn(var), z, mean);
         uint8_t *op = out + row * d_bytes;
