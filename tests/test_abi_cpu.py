@@ -485,3 +485,65 @@ def test_native_plan(lib):
                                                ctypes.byref(p)) == ga.ERR_DTYPE
     assert lib.gelu_and_mul_sparse_native_plan(0, 0x100000, 4, 64, 128, ga.BF16, GB300_SMS,
                                                None) == ga.ERR_NULL
+
+
+def _native_plan(lib, T, d, dtype, sms=GB300_SMS):
+    p = ga.Plan()
+    rc = lib.gelu_and_mul_sparse_native_plan(0x10000, 0x100000, T, d, 2 * d, dtype, sms,
+                                             ctypes.byref(p))
+    return rc, p.as_dict()
+
+
+@pytest.mark.parametrize("dtype", [ga.BF16, ga.F16, ga.F32])
+def test_plan_invariants_over_modes(lib, dtype):
+    """Every automatic plan -- each element type, plain and native rounding,
+    with and without a workspace, across row counts around the SM count and
+    its multiples -- is a launch the kernels can run: a legal block, a grid
+    that covers the rows, CTA slices that cover the row, shared memory within
+    the SM's limit, and only the geometries each mode has."""
+    elem = 4 if dtype == ga.F32 else 2
+    epv = 16 // elem
+    Ts = (1, 2, 8, 9, 19, 33, 64, 76, 77, 152, 153, 456, 1216, 1217, 2048, 4096)
+    ds = (64, 512, 1000, 2048, 4096, 6144, 8192, 9216, 11008, 14336, 16384, 20480, 24576,
+          28672, 32768, 65536)
+    modes = [("plain", 0), ("plain", 1)] + ([("native", 0)] if dtype != ga.F32 else [])
+    for mode, ws in modes:
+        for T in Ts:
+            for d in ds:
+                if mode == "native":
+                    rc, p = _native_plan(lib, T, d, dtype)
+                else:
+                    rc, p = plan(lib, T, d, dtype=dtype, ws=ws)
+                where = (mode, ws, T, d, p)
+                assert rc == 0, where
+                v, nt, grid = p["variant"], p["threads"], p["grid"]
+                assert 32 <= nt <= 1024 and nt % 32 == 0, where
+                assert 1 <= grid <= 0x7FFFFFFF, where
+                nvec = d // epv
+                if d % epv:
+                    assert v == "scalar", where
+                    continue
+                if dtype != ga.BF16 or mode == "native":
+                    # warp rows and the bulk-copy kernels are plain bf16 only
+                    assert v in ("cta_row", "split_rows", "scalar"), where
+                if v in ("tma_rows", "pipe_rows"):
+                    cover = (nt - (32 if v == "pipe_rows" else 0)) * p["vec_per_thread"]
+                    assert cover >= nvec, where
+                    assert grid <= min(T, GB300_SMS * p["ctas_per_sm"]), where
+                    assert p["smem_bytes"] * p["ctas_per_sm"] <= 228 * 1024, where
+                    assert p["dynamic_rows"] in (0, 1), where
+                else:
+                    assert p["dynamic_rows"] == 0 and p["smem_bytes"] == 0, where
+                if v == "split_rows":
+                    assert p["cluster"] in (2, 4, 8) and grid == T * p["cluster"], where
+                    assert grid <= GB300_SMS and nt * p["vec_per_thread"] >= nvec, where
+                elif v == "cta_row":
+                    sv = -(-nvec // p["cluster"])
+                    assert p["cluster"] in (1, 2, 4, 8), where
+                    assert nt * p["vec_per_thread"] >= sv, where
+                    assert grid == T * p["cluster"], where
+                elif v == "warp_rows":
+                    assert 32 * p["vec_per_thread"] >= nvec, where
+                    assert grid * p["rows_per_cta"] >= T, where
+                elif v == "scalar":
+                    assert grid == T, where
