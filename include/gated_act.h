@@ -264,8 +264,11 @@ int gelu_and_mul_sparse_plan_ex(const void *out, const void *in, int64_t T,
  *            in [1, 8]; for GATED_ACT_VARIANT_TMA_ROWS: CTAs per SM, a power
  *            of two in [1, 16] (threads per CTA = 1024 / that); for
  *            GATED_ACT_VARIANT_PIPE_ROWS: CTAs per SM, a power of two in
- *            [1, 8]; 0 lets the library choose; ignored by the other
- *            variants.
+ *            [1, 8]; 0 lets the library choose for those three; for
+ *            GATED_ACT_VARIANT_SPLIT_ROWS: CTAs per row, 2, 4 or 8 (no
+ *            default: other values return GATED_ACT_ERR_VARIANT; device
+ *            memory and rows of up to 4096 16-byte vectors only); ignored by
+ *            the other variants.
  * Returns GATED_ACT_ERR_VARIANT when the layout cannot use that geometry
  * (vector variants need the 16-byte layout above; a row slice must fit the
  * CTA's registers).
@@ -281,8 +284,8 @@ int gelu_and_mul_sparse_ex(void *out, const void *in, int64_t T, int64_t d,
  *   dtype    a gated_act_dtype shared by in and out.  Sizes and strides are
  *            in elements; pointers aligned to the element size.
  *   variant, cluster as in gelu_and_mul_sparse_ex.  fp16 and fp32 run the
- *            CTA-row (or scalar) geometry only: WARP_ROWS and TMA_ROWS
- *            return GATED_ACT_ERR_VARIANT for them.
+ *            CTA-row, split-row or scalar geometries only: WARP_ROWS,
+ *            TMA_ROWS and PIPE_ROWS return GATED_ACT_ERR_VARIANT for them.
  * Math is fp32 throughout; the fp32 output evaluates tanh-GELU as
  * s / (1 + e^{-2y}) on the hardware exponential and reciprocal (relative
  * error about 2^-21), the 16-bit outputs use the hardware tanh.  Accuracy against an fp64 evaluation:
