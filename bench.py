@@ -555,9 +555,7 @@ def run_ours(args, world, rank, local):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": STEP_WORKLOAD if not profiling else
-                       (f"gelu_and_mul_sparse T={args.only[0]} d={args.only[1]}" if args.only else
-                        f"silu_and_mul M={args.only_silu} d={launches[0]['d']}"),
+            "config": {"workload": workload_name(args, launches),
                        "launches_per_step": len(launches), "bytes_per_step": bytes_step,
                        "l2": "no flush: every launch has its own buffers (2.7 GB per step, "
                              "129 MB L2)",
@@ -579,6 +577,16 @@ STEP_WORKLOAD = ("gelu_and_mul_sparse T{1,8,64,256,1024,2048} x d{2048..32768} x
 TARGET_SHAPES = ((1024, 16384), (1024, 32768), (2048, 8192), (2048, 16384), (2048, 32768))
 DECODE_SHAPES = ((1, 8192), (8, 8192), (64, 8192))
 LINE_LIMIT = 2000
+
+
+def workload_name(args, launches) -> str:
+    """config.workload of both arms: the step's sweep, or the one shape that a
+    profiling run (--only, --only-silu) times."""
+    if args.only:
+        return f"gelu_and_mul_sparse T={args.only[0]} d={args.only[1]}"
+    if args.only_silu:
+        return f"silu_and_mul M={args.only_silu} d={launches[0]['d']}"
+    return STEP_WORKLOAD
 
 
 def _shape_row(rows, T, d, z):
@@ -947,8 +955,11 @@ def run_reference(args, world, rank):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "impl": "reference",
-            "config": {"workload": "gelu_and_mul_sparse sweep + silu_and_mul MoE decode "
-                                   "(bounded row sample per step)", "rows_per_launch": R},
+            "config": {"workload": workload_name(args, launches),
+                       "launches_per_step": len(launches),
+                       "bytes_per_step": sum(L["bytes"] for L in launches),
+                       "parallelism": "the oracle on rank 0's host cores",
+                       "sample_rows_per_launch": R},
             "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": o.max_threads(),
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,

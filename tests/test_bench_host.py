@@ -98,6 +98,13 @@ def test_reference_arm_prints_one_json_line():
     assert j["impl"] == "reference" and j["metric"] == bench.METRIC and j["unit"] == "GB/s"
     assert j["value"] > 0 and j["cpu_baseline"]["kind"] == "oracle"
     assert j["e2e"]["h2d_bytes_per_step"] == 0
+    # the same workload as the CUDA arm's line; the sample is in cpu_baseline
+    assert j["config"]["workload"] == bench.STEP_WORKLOAD
+    launches = bench.workload_launches(None, None)
+    assert j["config"]["bytes_per_step"] == sum(L["bytes"] for L in launches)
+    assert j["config"]["launches_per_step"] == len(launches) == 64
+    assert f"first min(T, {j['config']['sample_rows_per_launch']}) rows" in \
+        j["cpu_baseline"]["sample"]
 
 
 def test_cpu_model_names_arm_cores(monkeypatch):
