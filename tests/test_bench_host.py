@@ -194,3 +194,14 @@ def test_bench_line_is_short_and_last(capsys, tmp_path):
     # the side file keeps every row
     back = json.loads(detail.read_text())
     assert len(back["per_shape"]) == 64 and len(back["widened_rows"]) == len(bench.extra_launches())
+
+
+def test_workload_name_of_both_arms():
+    args = bench.parse_args([])
+    assert bench.workload_name(args, bench.workload_launches()) == bench.STEP_WORKLOAD
+    args = bench.parse_args(["--only", "2048,16384"])
+    assert bench.workload_name(args, bench.workload_launches(args.only)) == \
+        "gelu_and_mul_sparse T=2048 d=16384"
+    args = bench.parse_args(["--only-silu", "2048"])
+    L = bench.workload_launches(None, args.only_silu)
+    assert bench.workload_name(args, L) == "silu_and_mul M=2048 d=768"
